@@ -1,0 +1,192 @@
+/*
+ * mk.h -- C ABI of the GB300 persistent decode megakernel library (libmk.so).
+ *
+ * Batch-1 autoregressive decode of a Qwen3-style decoder run as ONE
+ * cooperatively launched kernel that loops over layers and decode steps
+ * without exiting ("launch one kernel that owns the GPU and loops over decode
+ * steps internally", page A section "The idea: one kernel that never exits").
+ *
+ * Sources cited below:
+ *   page A = "Porting a 1,200-line persistent CUDA megakernel to Qwen3-TTS:
+ *            ~25 ms to first audio chunk" (dev.to)
+ *   page B = "I made a single CUDA kernel speak: streaming Qwen3-TTS at 50ms
+ *            latency on an RTX 5090" (theaicatchup.com)
+ *
+ * Conventions for every entry point:
+ *   - Return value: MK_OK (0) or a negative MK_ERR_* code.  Nothing aborts the
+ *     process.  mk_error_string() names a code.
+ *   - "device" pointers are CUDA global-memory addresses on the handle's device
+ *     (the device current at mk_create); "host" pointers are ordinary host memory.
+ *   - Streams are passed as `mk_stream` (a cudaStream_t); NULL is the legacy
+ *     default stream.
+ *   - A handle is not thread-safe: one caller at a time.
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define MK_OK               0
+#define MK_ERR_INVALID_ARG (-1)  /* bad pointer, size or option, checked on the host */
+#define MK_ERR_UNSUPPORTED (-2)  /* shape or launch geometry this build does not handle */
+#define MK_ERR_KV_FULL     (-3)  /* position + forwards would pass max_seq (host check) */
+#define MK_ERR_BAD_TOKEN   (-4)  /* id >= vocab_in, or a sentinel row outside the buffer
+                                    (found on the device; later forwards are skipped) */
+#define MK_ERR_TIMEOUT     (-5)  /* a device wait (grid barrier, ring, merge) ran past
+                                    its time budget; the kernel returned early */
+#define MK_ERR_NUMERIC     (-6)  /* a logit was NaN or infinite */
+#define MK_ERR_CUDA        (-7)  /* a CUDA runtime call failed */
+#define MK_ERR_NO_MEMORY   (-8)  /* a device allocation failed */
+#define MK_ERR_BAD_POSITION (-9) /* an MRoPE position-stream value outside the rotary table */
+
+typedef struct mk_handle mk_handle;
+typedef void *mk_stream; /* cudaStream_t */
+
+/* ---- model description ---------------------------------------------------
+ * Qwen3-style decoder (page B, "Why Does a Single Kernel Even Matter for
+ * TTS?": the TTS talker "mirrors Qwen3-0.6B exactly -- same dims, layers,
+ * heads"; vocab, RoPE frequencies and the untied head differ).  The page's
+ * kernel bakes these into compile-time constants (page A, "Porting it to
+ * Qwen3-TTS-1.7B"); here they are runtime fields checked at mk_create, with
+ * head_dim a template parameter of the kernel.
+ *
+ * Limits checked by mk_create (MK_ERR_UNSUPPORTED otherwise):
+ *   head_dim in {64, 128}; n_q_heads % n_kv_heads == 0 with group size
+ *   n_q_heads / n_kv_heads in {1, 2, 4, 8} and group * head_dim <= 512;
+ *   every GEMV input width (hidden, n_q_heads * head_dim, intermediate) is
+ *   K = KPT * T with KPT in {8, 12, 16, 24} and T in {32, 64, 128, 256};
+ *   rope_mode 1 needs mrope_sections summing to head_dim / 2.             */
+typedef struct {
+  int32_t n_layers;
+  int32_t hidden;          /* H */
+  int32_t n_q_heads;       /* Hq */
+  int32_t n_kv_heads;      /* Hkv */
+  int32_t head_dim;        /* d */
+  int32_t intermediate;    /* I, SiLU-gated MLP width */
+  int32_t vocab;           /* V, rows of the LM head */
+  int32_t vocab_in;        /* rows of the input embedding table */
+  float rms_eps;           /* RMSNorm epsilon inside the root (Qwen3: 1e-6) */
+  float rope_theta;        /* rotary base (Qwen3: 1e6) */
+  int32_t rope_mode;       /* 0 = RoPE, 1 = sectioned MRoPE (page A, "Porting it to
+                              Qwen3-TTS-1.7B": "splits position encoding into sections") */
+  int32_t mrope_sections[3]; /* rotary pairs driven by position streams 0, 1, 2 */
+  int32_t max_seq;         /* KV-cache capacity in positions */
+  int32_t rope_positions;  /* rows of the host-built cos/sin table; 0 = 2*max_seq + 8
+                              ("RoPE freq? Python tables only", page B, "So, What's
+                              the Catch with These Megakernels?") */
+  uint32_t flags;          /* reserved, must be 0 */
+} mk_config;
+
+/* Per-layer weights: device pointers to bf16, row-major [out][in] (the
+ * torch.nn.Linear layout), each 16-byte aligned.  Norm gains are [H] or [d].
+ *   wq [Hq*d][H], wk/wv [Hkv*d][H], wo [H][Hq*d],
+ *   w_gate/w_up [I][H], w_down [H][I].
+ * BORROWED: the caller keeps them alive and unchanged until mk_destroy. */
+typedef struct {
+  const void *attn_norm, *wq, *wk, *wv, *q_norm, *k_norm, *wo;
+  const void *mlp_norm, *w_gate, *w_up, *w_down;
+} mk_layer_weights;
+
+typedef struct {
+  const void *embed;      /* [vocab_in][H] bf16, device, borrowed */
+  const void *lm_head;    /* [vocab][H] bf16, or NULL = tied to embed (requires
+                             vocab == vocab_in); page A, "Porting it to Qwen3-TTS-1.7B":
+                             the text model ties them, the talker does not */
+  const void *final_norm; /* [H] bf16 */
+  const mk_layer_weights *layers; /* HOST array of n_layers entries, read at mk_create */
+} mk_weights;
+
+/* ---- per-call options (all optional; pass NULL for defaults) ------------ */
+#define MK_DECODE_PER_OP 1u  /* run the same math as one ordinary kernel launch per
+                                phase (the launch-overhead ablation; page A, "The idea":
+                                a conventional step "launches a long chain of kernels") */
+
+typedef struct {
+  uint32_t flags;             /* MK_DECODE_* bits */
+  const float *embeds;        /* device [n_embed_rows][H] fp32 precomputed input rows;
+                                 id -(r+1) selects row r (page B, "Why Does a Single
+                                 Kernel Even Matter for TTS?": "If token_id >=0, lookup
+                                 embedding. Else, grab precomputed from buffer") */
+  int32_t n_embed_rows;
+  const int32_t *pos3;        /* device [3][n_in + n_steps] position streams for MRoPE;
+                                 NULL = the slot index in every stream */
+  float *logits;              /* device [n_in + n_steps][vocab] fp32 out, or NULL */
+  float *hidden;              /* device [n_in + n_steps][n_layers + 1][H] fp32 out, or NULL:
+                                 the input row then the residual stream after each layer */
+  uint64_t *trace;            /* device [n_fwd][5*n_layers + 1][grid] %globaltimer stamps
+                                 taken after each phase's grid barrier, or NULL */
+  int32_t attn_chunks;        /* split-KV chunks per kv head; 0 = grid / n_kv_heads */
+  int64_t spin_ns;            /* budget of every device wait; 0 = 1 s */
+  int32_t fault_skip_barrier; /* test hook: CTA 0 skips its arrival at this grid barrier
+                                 (0-based, persistent path only); -1 = off */
+} mk_decode_opts;
+
+typedef struct {
+  int32_t grid;          /* CTAs = SMs of the device, one per SM */
+  int32_t threads;       /* per CTA: consumer warps + 1 producer warp */
+  int32_t stages;        /* shared-memory ring stages */
+  int32_t stage_bytes;
+  int32_t smem_bytes;    /* dynamic shared memory per CTA */
+  int32_t position;      /* next KV slot */
+  int32_t max_chunks;    /* split-KV chunk capacity per kv head */
+  int64_t weight_bytes;  /* bf16 bytes streamed per forward (layers + head) */
+  int64_t kv_bytes;      /* KV-cache allocation */
+} mk_info;
+
+/* Validate cfg, allocate the KV cache [L][Hkv][max_seq][d] bf16 (keys and
+ * values), scratch, barrier/error words and the cos/sin table (built on the
+ * host in double precision), and check that one CTA per SM fits.  *out gets
+ * the handle.  Errors: MK_ERR_INVALID_ARG, MK_ERR_UNSUPPORTED, MK_ERR_NO_MEMORY,
+ * MK_ERR_CUDA (nothing is leaked on failure). */
+int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out);
+
+/* Forget the cached context: the cursor returns to slot 0 and the last id to 0.
+ * Enqueued on `stream`; returns after the stream completes. */
+int mk_reset_kv(mk_handle *h, mk_stream stream);
+
+/* Run n_in + n_steps forwards from the handle's cursor in ONE cooperative launch.
+ * Forward i < n_in consumes d_in_ids[i] (device int32; a negative id picks a
+ * row of opts->embeds); forward i >= n_in consumes the greedy id of forward
+ * i-1 (for i == 0, the last id of the previous call).  d_out_ids[i] (device
+ * int32, n_in + n_steps entries) receives the greedy argmax of forward i,
+ * lowest index on ties.  Blocks until `stream` completes and returns the
+ * device status.  After an error the cached context is undefined: call
+ * mk_reset_kv.  Errors: all codes above. */
+int mk_decode(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_steps,
+              int32_t *d_out_ids, const mk_decode_opts *opts, mk_stream stream);
+
+/* mk_decode with HOST id buffers: copies h_in_ids to the device, decodes and
+ * copies the ids back to h_out_ids (n_in + n_steps entries).  The copies use
+ * handle-owned staging; at most max_seq ids per call. */
+int mk_decode_host(mk_handle *h, const int32_t *h_in_ids, int32_t n_in, int32_t n_steps,
+                   int32_t *h_out_ids, const mk_decode_opts *opts, mk_stream stream);
+
+/* Launch geometry, cursor and byte counts of a handle. */
+int mk_get_info(const mk_handle *h, mk_info *info);
+
+/* Talker input rows: out[r] = sum_{j<n_books} books[j][codes[r][j]] + text[text_ids[r]],
+ * accumulated in fp32 in table order (page B, "Why Does a Single Kernel Even
+ * Matter for TTS?": inputs "are sums of 17 embeddings (16 codebooks + text)").
+ * books: device bf16 [n_books][book_rows][H]; text: device bf16 [text_rows][H];
+ * codes: device int32 [n][n_books]; text_ids: device int32 [n]; out: device fp32
+ * [n][H].  Ids out of range give MK_ERR_BAD_TOKEN.  Blocks until `stream` completes. */
+int mk_embed_sum(const void *books, int32_t n_books, int32_t book_rows, const void *text,
+                 int32_t text_rows, int32_t hidden, const int32_t *codes,
+                 const int32_t *text_ids, int32_t n, float *out, mk_stream stream);
+
+/* Free everything the handle owns (not the borrowed weights).  NULL is a no-op. */
+int mk_destroy(mk_handle *h);
+
+/* Static string naming a status code. */
+const char *mk_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MK_H */

@@ -1,0 +1,283 @@
+"""ctypes binding with the same names as the C ABI in ``include/mk.h``.
+
+Argument marshalling only: the structs below mirror ``mk_config``,
+``mk_layer_weights``, ``mk_weights``, ``mk_decode_opts`` and ``mk_info``; the
+``Decoder`` class owns one ``mk_handle`` plus the torch device tensors whose
+pointers the handle borrows.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+MK_DECODE_PER_OP = 1
+
+_ERRORS = {0: "ok", -1: "invalid argument", -2: "unsupported shape or launch geometry",
+           -3: "KV cache full", -4: "token id or sentinel row out of range",
+           -5: "device wait timed out", -6: "non-finite logit", -7: "CUDA runtime error",
+           -8: "device out of memory", -9: "position stream outside the rotary table"}
+
+
+class MKError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__("%s: %s (%d)" % (what, _ERRORS.get(code, "unknown"), code))
+        self.code = code
+
+
+class mk_config(C.Structure):
+    _fields_ = [("n_layers", C.c_int32), ("hidden", C.c_int32), ("n_q_heads", C.c_int32),
+                ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("intermediate", C.c_int32),
+                ("vocab", C.c_int32), ("vocab_in", C.c_int32), ("rms_eps", C.c_float),
+                ("rope_theta", C.c_float), ("rope_mode", C.c_int32),
+                ("mrope_sections", C.c_int32 * 3), ("max_seq", C.c_int32),
+                ("rope_positions", C.c_int32), ("flags", C.c_uint32)]
+
+
+class mk_layer_weights(C.Structure):
+    _fields_ = [(k, C.c_void_p) for k in ("attn_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo",
+                                          "mlp_norm", "w_gate", "w_up", "w_down")]
+
+
+class mk_weights(C.Structure):
+    _fields_ = [("embed", C.c_void_p), ("lm_head", C.c_void_p), ("final_norm", C.c_void_p),
+                ("layers", C.POINTER(mk_layer_weights))]
+
+
+class mk_decode_opts(C.Structure):
+    _fields_ = [("flags", C.c_uint32), ("embeds", C.c_void_p), ("n_embed_rows", C.c_int32),
+                ("pos3", C.c_void_p), ("logits", C.c_void_p), ("hidden", C.c_void_p),
+                ("trace", C.c_void_p), ("attn_chunks", C.c_int32), ("spin_ns", C.c_int64),
+                ("fault_skip_barrier", C.c_int32)]
+
+
+class mk_info(C.Structure):
+    _fields_ = [("grid", C.c_int32), ("threads", C.c_int32), ("stages", C.c_int32),
+                ("stage_bytes", C.c_int32), ("smem_bytes", C.c_int32), ("position", C.c_int32),
+                ("max_chunks", C.c_int32), ("weight_bytes", C.c_int64), ("kv_bytes", C.c_int64)]
+
+
+#: every symbol include/mk.h declares
+EXPORTS = ("mk_create", "mk_reset_kv", "mk_decode", "mk_decode_host", "mk_get_info",
+           "mk_embed_sum", "mk_destroy", "mk_error_string")
+
+_lib = None
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, "libmk.so")
+
+
+def load_library(path: Optional[str] = None):
+    """Load libmk.so (in-tree) and declare the C signatures.  Raises if absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or lib_path()
+    if not os.path.exists(p):
+        raise RuntimeError("libmk.so not built at %s: run __graft_entry__.build()" % p)
+    lib = C.CDLL(p)
+    vp, i32, i64 = C.c_void_p, C.c_int32, C.c_int64
+    lib.mk_create.argtypes = [C.POINTER(mk_config), C.POINTER(mk_weights), C.POINTER(vp)]
+    lib.mk_reset_kv.argtypes = [vp, vp]
+    lib.mk_decode.argtypes = [vp, vp, i32, i32, vp, C.POINTER(mk_decode_opts), vp]
+    lib.mk_decode_host.argtypes = [vp, vp, i32, i32, vp, C.POINTER(mk_decode_opts), vp]
+    lib.mk_get_info.argtypes = [vp, C.POINTER(mk_info)]
+    lib.mk_embed_sum.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, i32, vp, vp]
+    lib.mk_destroy.argtypes = [vp]
+    lib.mk_error_string.argtypes = [C.c_int]
+    lib.mk_error_string.restype = C.c_char_p
+    for name in EXPORTS:
+        if name != "mk_error_string":
+            getattr(lib, name).restype = C.c_int
+    del i64
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def error_string(code: int) -> str:
+    return load_library().mk_error_string(code).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise MKError(rc, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream) -> C.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _dev_bf16(bits: np.ndarray, device) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.to(device, non_blocking=False).contiguous()
+
+
+def _require_cuda():
+    if not torch.cuda.is_available():
+        raise RuntimeError("persistent_transformer_megakernel_gb300 needs a CUDA device (GB300)")
+
+
+class Decoder:
+    """One decode session: weights on the device, a KV cache, a cursor.
+
+    ``shape`` is a dict (see ``workloads.SHAPES``); ``weights`` holds bf16 bit
+    patterns as numpy ``uint16`` arrays (``workloads.make_weights``) or torch
+    bf16 tensors already on the device."""
+
+    def __init__(self, shape: dict, weights: dict, max_seq: int, rope_positions: int = 0,
+                 device="cuda:0"):
+        _require_cuda()
+        self.lib = load_library()
+        self.device = torch.device(device)
+        torch.cuda.set_device(self.device)
+        self.shape = dict(shape)
+        s = self.shape
+        conv = (lambda a: a) if isinstance(weights["embed"], torch.Tensor) else \
+            (lambda a: _dev_bf16(a, self.device))
+        self._keep = []
+
+        def dev(a):
+            t = conv(a)
+            self._keep.append(t)
+            return t
+
+        self.embed = dev(weights["embed"])
+        self.final_norm = dev(weights["final_norm"])
+        self.lm_head = None if weights.get("lm_head") is None else dev(weights["lm_head"])
+        L = s["n_layers"]
+        self._layers = (mk_layer_weights * L)()
+        for l, lw in enumerate(weights["layers"]):
+            for k in mk_layer_weights._fields_:
+                setattr(self._layers[l], k[0], dev(lw[k[0]]).data_ptr())
+        cfg = mk_config()
+        cfg.n_layers, cfg.hidden = L, s["hidden"]
+        cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim = s["n_q_heads"], s["n_kv_heads"], s["head_dim"]
+        cfg.intermediate, cfg.vocab, cfg.vocab_in = s["intermediate"], s["vocab"], s["vocab_in"]
+        cfg.rms_eps, cfg.rope_theta = s.get("rms_eps", 1e-6), s.get("rope_theta", 1e6)
+        ms = s.get("mrope_sections")
+        cfg.rope_mode = 0 if ms is None else 1
+        if ms is not None:
+            cfg.mrope_sections[0], cfg.mrope_sections[1], cfg.mrope_sections[2] = ms
+        cfg.max_seq, cfg.rope_positions, cfg.flags = max_seq, rope_positions, 0
+        w = mk_weights()
+        w.embed = self.embed.data_ptr()
+        w.lm_head = None if self.lm_head is None else self.lm_head.data_ptr()
+        w.final_norm = self.final_norm.data_ptr()
+        w.layers = self._layers
+        h = C.c_void_p()
+        _check(self.lib.mk_create(C.byref(cfg), C.byref(w), C.byref(h)), "mk_create")
+        self.h = h
+        self.max_seq = max_seq
+        self._out = torch.empty(max_seq, dtype=torch.int32, device=self.device)
+
+    # ---------------------------------------------------------------- basics
+    def info(self) -> dict:
+        i = mk_info()
+        _check(self.lib.mk_get_info(self.h, C.byref(i)), "mk_get_info")
+        return {k: getattr(i, k) for k, _ in mk_info._fields_}
+
+    @property
+    def position(self) -> int:
+        return self.info()["position"]
+
+    def reset(self, stream=None):
+        _check(self.lib.mk_reset_kv(self.h, _stream_ptr(stream)), "mk_reset_kv")
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.lib.mk_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ---------------------------------------------------------------- decode
+    def _opts(self, per_op, embeds, pos3, logits, hidden, trace, attn_chunks, spin_ns,
+              fault_skip_barrier):
+        o = mk_decode_opts()
+        o.flags = MK_DECODE_PER_OP if per_op else 0
+        o.embeds = _ptr(embeds)
+        o.n_embed_rows = 0 if embeds is None else embeds.shape[0]
+        o.pos3 = _ptr(pos3)
+        o.logits = _ptr(logits)
+        o.hidden = _ptr(hidden)
+        o.trace = _ptr(trace)
+        o.attn_chunks = attn_chunks
+        o.spin_ns = spin_ns
+        o.fault_skip_barrier = fault_skip_barrier
+        return o
+
+    def decode(self, in_ids=None, n_steps: int = 0, *, out: Optional[torch.Tensor] = None,
+               per_op: bool = False, embeds: Optional[torch.Tensor] = None,
+               pos3: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
+               hidden: Optional[torch.Tensor] = None, trace: Optional[torch.Tensor] = None,
+               attn_chunks: int = 0, spin_ns: int = 0, fault_skip_barrier: int = -1,
+               stream=None) -> torch.Tensor:
+        """``mk_decode``: ``in_ids`` (device int32 tensor, or a sequence moved to
+        the device) then ``n_steps`` greedy forwards.  Returns the ids tensor."""
+        if in_ids is None:
+            d_in = None
+            n_in = 0
+        else:
+            d_in = in_ids if isinstance(in_ids, torch.Tensor) else \
+                torch.as_tensor(np.asarray(in_ids, dtype=np.int32), device=self.device)
+            d_in = d_in.to(device=self.device, dtype=torch.int32).contiguous()
+            n_in = d_in.numel()
+        n = n_in + n_steps
+        if out is None:
+            out = torch.empty(max(n, 1), dtype=torch.int32, device=self.device)
+        for t, dt in ((embeds, torch.float32), (logits, torch.float32), (hidden, torch.float32),
+                      (pos3, torch.int32)):
+            if t is not None and (t.dtype != dt or not t.is_cuda or not t.is_contiguous()):
+                raise ValueError("option tensors must be contiguous device tensors of the right dtype")
+        o = self._opts(per_op, embeds, pos3, logits, hidden, trace, attn_chunks, spin_ns,
+                       fault_skip_barrier)
+        rc = self.lib.mk_decode(self.h, _ptr(d_in), n_in, n_steps, _ptr(out), C.byref(o),
+                                _stream_ptr(stream))
+        _check(rc, "mk_decode")
+        return out[:n]
+
+    def decode_host(self, in_ids: Sequence[int], n_steps: int = 0, *, per_op: bool = False,
+                    embeds=None, pos3=None, stream=None) -> np.ndarray:
+        """``mk_decode_host``: host id buffers in and out (the copies are part of the call)."""
+        ids = np.ascontiguousarray(np.asarray(in_ids, dtype=np.int32))
+        n = ids.size + n_steps
+        out = np.empty(max(n, 1), dtype=np.int32)
+        o = self._opts(per_op, embeds, pos3, None, None, None, 0, 0, -1)
+        rc = self.lib.mk_decode_host(self.h, ids.ctypes.data_as(C.c_void_p) if ids.size else None,
+                                     ids.size, n_steps, out.ctypes.data_as(C.c_void_p), C.byref(o),
+                                     _stream_ptr(stream))
+        _check(rc, "mk_decode_host")
+        return out[:n]
+
+
+def embed_sum(books: torch.Tensor, text: torch.Tensor, codes: torch.Tensor, text_ids: torch.Tensor,
+              out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """``mk_embed_sum``: per-step sum of codebook rows and a text row (fp32)."""
+    _require_cuda()
+    lib = load_library()
+    n_books, book_rows, H = books.shape
+    n = codes.shape[0]
+    if out is None:
+        out = torch.empty((n, H), dtype=torch.float32, device=books.device)
+    codes_i = codes.to(torch.int32).contiguous()
+    text_i = text_ids.to(torch.int32).contiguous()
+    rc = lib.mk_embed_sum(_ptr(books), n_books, book_rows, _ptr(text), text.shape[0], H,
+                          _ptr(codes_i), _ptr(text_i), n, _ptr(out), _stream_ptr(stream))
+    _check(rc, "mk_embed_sum")
+    return out

@@ -1,0 +1,901 @@
+// Device code of the persistent decode megakernel.
+//
+// One CTA per SM.  Warps 0..7 are consumers; warp 8 is the TMA producer, whose
+// lane 0 walks the CTA's fixed tile schedule (weight rows of every GEMV phase,
+// then KV-cache chunks of every attention phase, layer after layer, step after
+// step) and streams it through a multi-stage shared-memory ring with 1-D bulk
+// copies.  Weight streaming does not depend on the data, so the producer runs
+// ahead across grid barriers and decode steps while the consumers wait.
+//
+// Per forward (one token), the phases and their grid barriers are
+//   per layer: QKV (RMSNorm fused) | attention (QK-norm, RoPE/MRoPE, KV append,
+//              split-KV partials, last-arriving CTA merges) | O-proj + residual
+//              | RMSNorm + gate/up + SiLU*mul | down-proj + residual
+//   then:      final RMSNorm + LM head + per-CTA argmax candidates
+// and the next forward's first phase reduces the candidates (greedy argmax,
+// lowest index on ties) and feeds the id back in-kernel.
+//
+// page A = "Porting a 1,200-line persistent CUDA megakernel to Qwen3-TTS: ~25 ms
+// to first audio chunk" (dev.to); page B = "I made a single CUDA kernel speak:
+// streaming Qwen3-TTS at 50ms latency on an RTX 5090" (theaicatchup.com).
+#pragma once
+#include <cstdint>
+#include <climits>
+#include <cmath>
+
+#include "mk_params.h"
+#include "ptx.cuh"
+
+namespace mk {
+
+constexpr int CONS_BAR = 1;   // named barrier id used by the consumer warps
+constexpr int MK_ERR_BAD_TOKEN_D = -4;
+constexpr int MK_ERR_TIMEOUT_D = -5;
+constexpr int MK_ERR_NUMERIC_D = -6;
+constexpr int MK_ERR_BAD_POSITION_D = -9;
+
+__device__ __forceinline__ void set_err(const Params &p, int code) { atomicCAS(p.err, 0, code); }
+
+__device__ __forceinline__ volatile int &flag(SmemCtl &S, int i) {
+  return reinterpret_cast<volatile int *>(S.flags)[i];
+}
+
+__device__ __forceinline__ void cons_sync() { named_bar_sync(CONS_BAR, NCT); }
+
+__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+// round-to-nearest-even float -> bf16 bits (NaN kept quiet)
+__device__ __forceinline__ uint16_t f2bf(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return static_cast<uint16_t>((u >> 16) | 0x40u);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// balanced contiguous split of `total` items over G CTAs
+__device__ __forceinline__ void split_range(int total, int G, int cta, int &r0, int &r1) {
+  r0 = static_cast<int>((static_cast<long long>(total) * cta) / G);
+  r1 = static_cast<int>((static_cast<long long>(total) * (cta + 1)) / G);
+}
+
+// Reduce N row-partials held by every lane to one full sum per row: after the
+// halving steps lane l holds row (l >> (5 - log2 N)), summed over the warp.
+template <int N>
+__device__ __forceinline__ float warp_multi_reduce(float (&v)[N], int lane) {
+  constexpr int LOGN = (N >= 16) ? 4 : (N >= 8) ? 3 : (N >= 4) ? 2 : (N >= 2) ? 1 : 0;
+#pragma unroll
+  for (int lvl = 0; lvl < LOGN; ++lvl) {
+    const int o = 16 >> lvl;
+    const int n = N >> lvl;
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      float send = up ? v[i] : v[i + n / 2];
+      float keep = up ? v[i + n / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+#pragma unroll
+  for (int o = 16 >> LOGN; o >= 1; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+  return v[0];
+}
+
+// ---------------------------------------------------------------------------
+// waits (every wait has a time budget; on expiry the CTA is marked aborted and
+// the caller carries on without blocking so that named barriers stay matched)
+// ---------------------------------------------------------------------------
+struct Deadline {
+  unsigned long long start = 0;
+  __device__ __forceinline__ bool expired(long long budget) {
+    unsigned long long now = globaltimer();
+    if (start == 0) { start = now; return false; }
+    return static_cast<long long>(now - start) > budget;
+  }
+};
+
+__device__ __forceinline__ void wait_full(const Params &p, SmemCtl &S, int slot, uint32_t parity) {
+  if (mbar_try_wait(&S.full[slot], parity)) return;
+  Deadline dl;
+  int n = 0;
+  while (!mbar_try_wait(&S.full[slot], parity)) {
+    if ((++n & 63) == 0) {
+      if (flag(S, F_ABORT)) return;
+      if (dl.expired(p.spin_ns)) { set_err(p, MK_ERR_TIMEOUT_D); flag(S, F_ABORT) = 1; return; }
+    }
+  }
+}
+
+// grid-wide barrier over all CTAs (consumer threads only); returns false when
+// the CTA must stop (timeout, or an error set by any CTA before arriving)
+static __device__ bool grid_barrier(const Params &p, SmemCtl &S, unsigned &target, int bar_index, int cta) {
+  cons_sync();
+  if (threadIdx.x == 0) {
+    target += static_cast<unsigned>(p.G);
+    const bool skip = (p.fault_barrier == bar_index) && (cta == 0);   // test hook
+    if (!skip) {
+      __threadfence();
+      red_release_add(p.bar, 1u);
+    }
+    if (!flag(S, F_ABORT)) {
+      Deadline dl;
+      int n = 0;
+      while (ld_acquire(p.bar) < target) {
+        if ((++n & 255) == 0 && dl.expired(p.spin_ns)) {
+          set_err(p, MK_ERR_TIMEOUT_D);
+          flag(S, F_ABORT) = 1;
+          break;
+        }
+      }
+    }
+    if (ld_relaxed_i32(p.err) != 0) flag(S, F_ABORT) = 1;
+  }
+  cons_sync();
+  return flag(S, F_ABORT) == 0;
+}
+
+// ---------------------------------------------------------------------------
+// argmax helpers (largest value, lowest index among equals)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+// block-wide argmax over the consumer threads; every consumer gets the result
+static __device__ void block_argmax(SmemCtl &S, float &v, int &i) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (better(ov, oi, v, i)) { v = ov; i = oi; }
+  }
+  if (lane == 0) { S.bestv[w] = v; S.besti[w] = i; }
+  cons_sync();
+  v = S.bestv[0];
+  i = S.besti[0];
+  for (int k = 1; k < NCW; ++k)
+    if (better(S.bestv[k], S.besti[k], v, i)) { v = S.bestv[k]; i = S.besti[k]; }
+  cons_sync();
+}
+
+// reduce the per-CTA LM-head candidates of the previous forward -> greedy id
+static __device__ int select_token(const Params &p, SmemCtl &S, int f_prev, int cta, bool final) {
+  float v = -INFINITY;
+  int i = INT_MAX;
+  for (int c = threadIdx.x; c < p.G; c += NCT) {
+    float cv = __ldcg(p.cand_val + c);
+    int ci = __ldcg(p.cand_idx + c);
+    if (better(cv, ci, v, i)) { v = cv; i = ci; }
+  }
+  block_argmax(S, v, i);
+  if (threadIdx.x == 0 && cta == 0) {
+    p.out_ids[f_prev] = i;
+    if (final) *p.last_id = i;
+  }
+  return i;
+}
+
+// ---------------------------------------------------------------------------
+// GEMV phases
+// ---------------------------------------------------------------------------
+template <int KPT>
+__device__ __forceinline__ void load_f32(const float *src, float (&xr)[KPT]) {
+  const float4 *s4 = reinterpret_cast<const float4 *>(src);
+#pragma unroll
+  for (int c = 0; c < KPT / 4; ++c) {
+    float4 q = __ldcg(s4 + c);
+    xr[4 * c] = q.x; xr[4 * c + 1] = q.y; xr[4 * c + 2] = q.z; xr[4 * c + 3] = q.w;
+  }
+}
+
+template <int KPT>
+__device__ __forceinline__ void load_bf16(const uint16_t *src, float (&xr)[KPT]) {
+  const uint2 *s2 = reinterpret_cast<const uint2 *>(src);
+#pragma unroll
+  for (int c = 0; c < KPT / 4; ++c) {
+    uint2 q = __ldg(s2 + c);
+    xr[4 * c] = bf_lo(q.x); xr[4 * c + 1] = bf_hi(q.x);
+    xr[4 * c + 2] = bf_lo(q.y); xr[4 * c + 3] = bf_hi(q.y);
+  }
+}
+
+// dot of KPT bf16 weights in shared memory with the register slice
+template <int KPT>
+__device__ __forceinline__ float dot_row(const unsigned char *src, const float (&xr)[KPT]) {
+  float s = 0.f;
+  if constexpr (KPT % 8 == 0) {
+#pragma unroll
+    for (int c = 0; c < KPT / 8; ++c) {
+      uint4 q = *reinterpret_cast<const uint4 *>(src + 16 * c);
+      s = fmaf(bf_lo(q.x), xr[8 * c + 0], s);
+      s = fmaf(bf_hi(q.x), xr[8 * c + 1], s);
+      s = fmaf(bf_lo(q.y), xr[8 * c + 2], s);
+      s = fmaf(bf_hi(q.y), xr[8 * c + 3], s);
+      s = fmaf(bf_lo(q.z), xr[8 * c + 4], s);
+      s = fmaf(bf_hi(q.z), xr[8 * c + 5], s);
+      s = fmaf(bf_lo(q.w), xr[8 * c + 6], s);
+      s = fmaf(bf_hi(q.w), xr[8 * c + 7], s);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < KPT / 4; ++c) {
+      uint2 q = *reinterpret_cast<const uint2 *>(src + 8 * c);
+      s = fmaf(bf_lo(q.x), xr[4 * c + 0], s);
+      s = fmaf(bf_hi(q.x), xr[4 * c + 1], s);
+      s = fmaf(bf_lo(q.y), xr[4 * c + 2], s);
+      s = fmaf(bf_hi(q.y), xr[4 * c + 3], s);
+    }
+  }
+  return s;
+}
+
+// Input row of forward f: a non-negative id reads the embedding table, a
+// negative id -(r+1) row r of the caller's precomputed fp32 buffer (page B,
+// "Why Does a Single Kernel Even Matter for TTS?", the sentinel).
+template <int KPT>
+__device__ __forceinline__ void load_input_slice(const Params &p, int id, int k0, float (&xr)[KPT]) {
+  if (id >= 0) load_bf16<KPT>(p.embed + static_cast<size_t>(id) * p.H + k0, xr);
+  else load_f32<KPT>(p.embeds + static_cast<size_t>(-id - 1) * p.H + k0, xr);
+}
+
+__device__ __forceinline__ float input_elem(const Params &p, int id, int k) {
+  return id >= 0 ? bf2f(p.embed[static_cast<size_t>(id) * p.H + k])
+                 : p.embeds[static_cast<size_t>(-id - 1) * p.H + k];
+}
+
+// One GEMV phase of this CTA: y[r] = W[r,:] . in for the CTA's rows, with the
+// RMSNorm of the input fused in (QKV, gate/up, LM head) and the phase's
+// epilogue (store, residual add, SiLU*mul, logits + argmax candidate).
+template <int KPT, int RPTP>
+__device__ void gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer, int f,
+                           int cta, int in_id, uint32_t &it, int &rb) {
+  const GemvGeom g = p.geo[kind];
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int kc = t % g.TPR, rg = t / g.TPR;
+  const int k0 = kc * KPT;
+
+  // ---- input slice into registers ------------------------------------------
+  float xr[KPT];
+  if (kind == GV_QKV && layer == 0) load_input_slice<KPT>(p, in_id, k0, xr);
+  else if (kind == GV_O) load_f32<KPT>(p.attn + k0, xr);
+  else if (kind == GV_DOWN) load_f32<KPT>(p.u + k0, xr);
+  else load_f32<KPT>(p.x + k0, xr);
+
+  if (kind == GV_QKV || kind == GV_GU || kind == GV_LM) {
+    // RMSNorm fused into the GEMV: every CTA reduces mean(x^2) itself
+    float ss = 0.f;
+    if (rg == 0) {
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) ss = fmaf(xr[j], xr[j], ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) S.misc[w] = ss;
+    cons_sync();
+    float tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < NCW; ++i) tot += S.misc[i];
+    const float rs = 1.0f / sqrtf(tot / static_cast<float>(g.K) + p.eps);
+    const uint16_t *gain = kind == GV_QKV ? p.layers[layer].attn_norm
+                         : kind == GV_GU  ? p.layers[layer].mlp_norm
+                                          : p.final_norm;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) xr[j] = xr[j] * rs * bf2f(gain[k0 + j]);
+  }
+
+  // the first layer's input also seeds the residual stream (rows this CTA owns)
+  if (kind == GV_QKV && layer == 0) {
+    int o0, o1;
+    split_range(p.H, p.G, cta, o0, o1);
+    for (int r = o0 + t; r < o1; r += NCT) {
+      float v = input_elem(p, in_id, r);
+      p.x[r] = v;
+      if (p.hidden) p.hidden[(static_cast<size_t>(f) * (p.L + 1)) * p.H + r] = v;
+    }
+  }
+
+  int r0, r1;
+  split_range(g.rows, p.G, cta, r0, r1);
+  const int ntiles = (r1 - r0 + g.RT - 1) / g.RT;
+  constexpr int LOGR = (RPTP >= 16) ? 4 : (RPTP >= 8) ? 3 : (RPTP >= 4) ? 2 : (RPTP >= 2) ? 1 : 0;
+  const int wpr = g.TPR / 32;
+  float best_v = -INFINITY;
+  int best_i = INT_MAX;
+
+  for (int ti = 0; ti < ntiles; ++ti) {
+    const int a = r0 + ti * g.RT;
+    const int nr = min(g.RT, r1 - a);
+    const int rows_in_tile = (kind == GV_GU) ? 2 * nr : nr;
+    const int slot = static_cast<int>(it % static_cast<uint32_t>(p.stages));
+    const uint32_t par = (it / static_cast<uint32_t>(p.stages)) & 1u;
+    wait_full(p, S, slot, par);
+    const unsigned char *st = ring + static_cast<size_t>(slot) * p.stage_bytes;
+    float acc[RPTP];
+#pragma unroll
+    for (int i = 0; i < RPTP; ++i) {
+      const int row = rg + i * g.NG;
+      acc[i] = 0.f;
+      if (row < rows_in_tile) acc[i] = dot_row<KPT>(st + (static_cast<size_t>(row) * g.K + k0) * 2, xr);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[slot]);
+    const float v = warp_multi_reduce<RPTP>(acc, lane);
+    if ((lane & ((32 >> LOGR) - 1)) == 0) S.red[rb][w][lane >> (5 - LOGR)] = v;
+    cons_sync();
+    if (t < nr) {
+      auto rowsum = [&](int row) {
+        const int gq = row % g.NG, si = row / g.NG;
+        float s = 0.f;
+        for (int ww = 0; ww < wpr; ++ww) s += S.red[rb][gq * wpr + ww][si];
+        return s;
+      };
+      const float y = rowsum(t);
+      const int grow = a + t;
+      switch (kind) {
+        case GV_QKV: p.qkv[grow] = y; break;
+        case GV_O: {
+          const float xn = __ldcg(p.x + grow) + y;
+          p.x[grow] = xn;
+          break;
+        }
+        case GV_GU: {
+          const float up = rowsum(nr + t);
+          p.u[grow] = y / (1.0f + expf(-y)) * up;     // SiLU(gate) * up
+          break;
+        }
+        case GV_DOWN: {
+          const float xn = __ldcg(p.x + grow) + y;
+          p.x[grow] = xn;
+          if (p.hidden) p.hidden[(static_cast<size_t>(f) * (p.L + 1) + layer + 1) * p.H + grow] = xn;
+          break;
+        }
+        default: {  // LM head
+          if (p.logits) p.logits[static_cast<size_t>(f) * p.V + grow] = y;
+          if (!isfinite(y)) set_err(p, MK_ERR_NUMERIC_D);
+          if (y > best_v) { best_v = y; best_i = grow; }
+          break;
+        }
+      }
+    }
+    rb ^= 1;
+    ++it;
+  }
+
+  if (kind == GV_LM) {
+    block_argmax(S, best_v, best_i);
+    if (t == 0) {
+      p.cand_val[cta] = best_v;
+      p.cand_idx[cta] = best_i;
+    }
+  }
+}
+
+// dispatch on (KPT, RPTP) fixed at mk_create
+static __device__ void gemv_dispatch(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer, int f,
+                              int cta, int in_id, uint32_t &it, int &rb) {
+  const int kpt = p.geo[kind].KPT, r = p.geo[kind].RPTP;
+#define MK_GEMV_CASE(KP, RP) \
+  if (kpt == KP && r == RP) { gemv_phase<KP, RP>(p, S, ring, kind, layer, f, cta, in_id, it, rb); return; }
+#define MK_GEMV_KPT(KP) \
+  MK_GEMV_CASE(KP, 1) MK_GEMV_CASE(KP, 2) MK_GEMV_CASE(KP, 4) MK_GEMV_CASE(KP, 8) MK_GEMV_CASE(KP, 16)
+  MK_GEMV_KPT(8)
+  MK_GEMV_KPT(12)
+  MK_GEMV_KPT(16)
+  MK_GEMV_KPT(24)
+#undef MK_GEMV_KPT
+#undef MK_GEMV_CASE
+}
+
+// ---------------------------------------------------------------------------
+// attention phase
+// ---------------------------------------------------------------------------
+struct AttnSched {
+  int P, ctx, cs, C, units;
+};
+
+__device__ __forceinline__ AttnSched attn_sched(const Params &p, int f) {
+  AttnSched a;
+  a.P = p.pos0 + f;
+  a.ctx = a.P + 1;
+  int cmax = p.chunks_override > 0 ? p.chunks_override : max(1, p.G / p.Hkv);
+  cmax = min(cmax, p.max_chunks);
+  a.cs = (a.ctx + cmax - 1) / cmax;
+  a.C = (a.ctx + a.cs - 1) / a.cs;
+  a.units = p.Hkv * a.C;
+  return a;
+}
+
+// rotary stream of pair i (page A, "Porting it to Qwen3-TTS-1.7B": MRoPE
+// sections; contiguous runs of pair indices per position stream)
+__device__ __forceinline__ int pair_stream(const Params &p, int i) {
+  if (p.rope_mode == 0) return 0;
+  return i < p.sec_b0 ? 0 : (i < p.sec_b1 ? 1 : 2);
+}
+
+__device__ __forceinline__ int stream_pos(const Params &p, int f, int s, int P) {
+  int pos = p.pos3 ? p.pos3[static_cast<size_t>(s) * p.n_fwd + f] : P;
+  if (pos < 0 || pos >= p.rope_len) {
+    set_err(p, MK_ERR_BAD_POSITION_D);
+    pos = 0;
+  }
+  return pos;
+}
+
+// One warp normalises (RMS over head_dim, times gain) and rotates one head
+// vector.  Lane l holds elements l + 32k so that the rotate-half partner of
+// element i (i + d/2) sits in the same lane.
+template <int HD>
+__device__ __forceinline__ void norm_rope_head(const Params &p, float (&v)[HD / 32], const uint16_t *gain,
+                                               int f, int P, bool rotate) {
+  constexpr int EPL = HD / 32;
+  const int lane = threadIdx.x & 31;
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < EPL; ++k) ss = fmaf(v[k], v[k], ss);
+  ss = warp_sum(ss);
+  const float rs = 1.0f / sqrtf(ss / static_cast<float>(HD) + p.eps);
+#pragma unroll
+  for (int k = 0; k < EPL; ++k) v[k] = v[k] * rs * bf2f(gain[lane + 32 * k]);
+  if (!rotate) return;
+#pragma unroll
+  for (int k = 0; k < EPL / 2; ++k) {
+    const int i = lane + 32 * k;                         // pair index < d/2
+    const int pos = stream_pos(p, f, pair_stream(p, i), P);
+    const float2 cs = p.rope[static_cast<size_t>(pos) * (HD / 2) + i];
+    const float a = v[k], b = v[k + EPL / 2];
+    v[k] = a * cs.x - b * cs.y;
+    v[k + EPL / 2] = b * cs.x + a * cs.y;
+  }
+}
+
+template <int HD, int GRP>
+__device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring, int l, int f, int cta,
+                                uint32_t &it) {
+  constexpr int EPL = HD / 32;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const AttnSched as = attn_sched(p, f);
+  const int P = as.P;
+  const int TP = p.stage_bytes / (4 * HD);     // positions per ring tile (K rows + V rows)
+  const LayerPtrs &LW = p.layers[l];
+
+  for (int u = cta; u < as.units; u += p.G) {
+    const int g = u / as.C, c = u % as.C;
+    const int a = c * as.cs, b = min(a + as.cs, as.ctx);
+    const int pend = min(b, P);                // positions < P come through the ring
+    const bool has_cur = (b == as.ctx);        // this chunk holds the new position P
+    cons_sync();                               // shared scratch reuse across units
+
+    // ---- QK-norm + RoPE of the group's queries; append K/V of position P ----
+    const int njobs = GRP + (has_cur ? 2 : 0);
+    for (int job = w; job < njobs; job += NCW) {
+      float v[EPL];
+      if (job < GRP) {
+        const int j = g * GRP + job;
+#pragma unroll
+        for (int k = 0; k < EPL; ++k) v[k] = __ldcg(p.qkv + j * HD + lane + 32 * k);
+        norm_rope_head<HD>(p, v, LW.q_norm, f, P, true);
+#pragma unroll
+        for (int k = 0; k < EPL; ++k) S.qs[job * HD + lane + 32 * k] = v[k] * p.inv_sqrt_d;
+      } else if (job == GRP) {
+        const float *src = p.qkv + p.Hq * HD + g * HD;
+#pragma unroll
+        for (int k = 0; k < EPL; ++k) v[k] = __ldcg(src + lane + 32 * k);
+        norm_rope_head<HD>(p, v, LW.k_norm, f, P, true);
+        uint16_t *dst = p.kcache + ((static_cast<size_t>(l) * p.Hkv + g) * p.max_seq + P) * HD;
+#pragma unroll
+        for (int k = 0; k < EPL; ++k) {
+          const uint16_t bb = f2bf(v[k]);
+          dst[lane + 32 * k] = bb;
+          S.kcur[lane + 32 * k] = bf2f(bb);
+        }
+        fence_proxy_async_global();
+      } else {
+        const float *src = p.qkv + (p.Hq + p.Hkv) * HD + g * HD;
+        uint16_t *dst = p.vcache + ((static_cast<size_t>(l) * p.Hkv + g) * p.max_seq + P) * HD;
+#pragma unroll
+        for (int k = 0; k < EPL; ++k) {
+          const uint16_t bb = f2bf(__ldcg(src + lane + 32 * k));
+          dst[lane + 32 * k] = bb;
+          S.vcur[lane + 32 * k] = bf2f(bb);
+        }
+        fence_proxy_async_global();
+      }
+    }
+    cons_sync();
+
+    // ---- scores and online softmax, one warp per position --------------------
+    float q[GRP][EPL], o[GRP][EPL], m[GRP], ls[GRP];
+#pragma unroll
+    for (int h = 0; h < GRP; ++h) {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) { q[h][e] = S.qs[h * HD + lane * EPL + e]; o[h][e] = 0.f; }
+      m[h] = -INFINITY;
+      ls[h] = 0.f;
+    }
+    auto visit = [&](const float (&kk)[EPL], const float (&vv)[EPL]) {
+#pragma unroll
+      for (int h = 0; h < GRP; ++h) {
+        float s = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) s = fmaf(q[h][e], kk[e], s);
+        s = warp_sum(s);
+        const float mn = fmaxf(m[h], s);
+        const float sc = expf(m[h] - mn);
+        const float pe = expf(s - mn);
+        ls[h] = ls[h] * sc + pe;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[h][e] = fmaf(pe, vv[e], o[h][e] * sc);
+        m[h] = mn;
+      }
+    };
+    for (int p0 = a; p0 < pend; p0 += TP) {
+      const int np = min(TP, pend - p0);
+      const int slot = static_cast<int>(it % static_cast<uint32_t>(p.stages));
+      const uint32_t par = (it / static_cast<uint32_t>(p.stages)) & 1u;
+      wait_full(p, S, slot, par);
+      const unsigned char *st = ring + static_cast<size_t>(slot) * p.stage_bytes;
+      for (int i = w; i < np; i += NCW) {
+        float kk[EPL], vv[EPL];
+        const uint16_t *kr = reinterpret_cast<const uint16_t *>(st) + static_cast<size_t>(i) * HD + lane * EPL;
+        const uint16_t *vr = reinterpret_cast<const uint16_t *>(st) + static_cast<size_t>(np + i) * HD + lane * EPL;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) { kk[e] = bf2f(kr[e]); vv[e] = bf2f(vr[e]); }
+        visit(kk, vv);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[slot]);
+      ++it;
+    }
+    if (has_cur && w == NCW - 1) {
+      float kk[EPL], vv[EPL];
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) { kk[e] = S.kcur[lane * EPL + e]; vv[e] = S.vcur[lane * EPL + e]; }
+      visit(kk, vv);
+    }
+
+    // ---- merge the 8 warps, then the chunks ---------------------------------
+#pragma unroll
+    for (int h = 0; h < GRP; ++h) {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) S.ow[w][h * HD + lane * EPL + e] = o[h][e];
+      if (lane == 0) { S.mw[w][h] = m[h]; S.lw[w][h] = ls[h]; }
+    }
+    cons_sync();
+    for (int e = t; e < GRP * HD; e += NCT) {
+      const int h = e / HD, i = e % HD;
+      float M = -INFINITY;
+      for (int ww = 0; ww < NCW; ++ww) M = fmaxf(M, S.mw[ww][h]);
+      float os = 0.f, lsum = 0.f;
+      for (int ww = 0; ww < NCW; ++ww) {
+        const float sc = expf(S.mw[ww][h] - M);
+        os = fmaf(sc, S.ow[ww][e], os);
+        lsum = fmaf(sc, S.lw[ww][h], lsum);
+      }
+      const int j = g * GRP + h;
+      if (as.C == 1) {
+        p.attn[j * HD + i] = os / lsum;
+      } else {
+        float *dst = p.part + (static_cast<size_t>(j) * p.max_chunks + c) * (HD + 2);
+        dst[i] = os;
+        if (i == 0) { dst[HD] = M; dst[HD + 1] = lsum; }
+      }
+    }
+    if (as.C > 1) {
+      // the last CTA to finish a chunk of kv head g merges all C chunks
+      cons_sync();
+      if (t == 0) {
+        __threadfence();
+        const unsigned old = atomicAdd(p.tickets + g, 1u);
+        const int last = (old == static_cast<unsigned>(as.C - 1)) ? 1 : 0;
+        if (last) {
+          atomicExch(p.tickets + g, 0u);
+          __threadfence();
+        }
+        flag(S, F_LAST) = last;
+      }
+      cons_sync();
+      if (flag(S, F_LAST)) {
+        for (int e = t; e < GRP * HD; e += NCT) {
+          const int h = e / HD, i = e % HD;
+          const int j = g * GRP + h;
+          const float *src = p.part + static_cast<size_t>(j) * p.max_chunks * (HD + 2);
+          float M = -INFINITY;
+          for (int cc = 0; cc < as.C; ++cc) M = fmaxf(M, __ldcg(src + cc * (HD + 2) + HD));
+          float os = 0.f, lsum = 0.f;
+          for (int cc = 0; cc < as.C; ++cc) {
+            const float sc = expf(__ldcg(src + cc * (HD + 2) + HD) - M);
+            os = fmaf(sc, __ldcg(src + cc * (HD + 2) + i), os);
+            lsum = fmaf(sc, __ldcg(src + cc * (HD + 2) + HD + 1), lsum);
+          }
+          p.attn[j * HD + i] = os / lsum;
+        }
+      }
+    }
+  }
+}
+
+template <int HD>
+__device__ void attention_dispatch(const Params &p, SmemCtl &S, unsigned char *ring, int l, int f, int cta,
+                                   uint32_t &it) {
+  switch (p.grp) {
+    case 1: attention_phase<HD, 1>(p, S, ring, l, f, cta, it); break;
+    case 2: attention_phase<HD, 2>(p, S, ring, l, f, cta, it); break;
+    case 4: attention_phase<HD, 4>(p, S, ring, l, f, cta, it); break;
+    default: attention_phase<HD, 8>(p, S, ring, l, f, cta, it); break;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// producer: walks the same tile schedule as the consumers
+// ---------------------------------------------------------------------------
+struct Producer {
+  const Params &p;
+  SmemCtl &S;
+  unsigned char *ring;
+  uint64_t pol_w, pol_kv;
+  uint32_t it = 0;
+  bool stop = false;
+
+  __device__ Producer(const Params &pp, SmemCtl &SS, unsigned char *r) : p(pp), S(SS), ring(r) {
+    pol_w = policy_evict_first();
+    pol_kv = policy_evict_normal();
+  }
+
+  // claim the next ring slot (waits until the consumers released it)
+  __device__ unsigned char *claim(int &slot) {
+    slot = static_cast<int>(it % static_cast<uint32_t>(p.stages));
+    const uint32_t k = it / static_cast<uint32_t>(p.stages);
+    if (k > 0) {
+      const uint32_t par = (k - 1) & 1u;
+      if (!mbar_try_wait(&S.empty[slot], par)) {
+        Deadline dl;
+        int n = 0;
+        while (!mbar_try_wait(&S.empty[slot], par)) {
+          if ((++n & 63) == 0) {
+            if (flag(S, F_ABORT)) { stop = true; return nullptr; }
+            if (dl.expired(p.spin_ns)) { set_err(p, MK_ERR_TIMEOUT_D); stop = true; return nullptr; }
+          }
+        }
+      }
+    }
+    if (flag(S, F_ABORT)) { stop = true; return nullptr; }
+    return ring + static_cast<size_t>(slot) * p.stage_bytes;
+  }
+
+  __device__ void gemv_tiles(int kind, int layer, int cta) {
+    const GemvGeom g = p.geo[kind];
+    int r0, r1;
+    split_range(g.rows, p.G, cta, r0, r1);
+    const uint32_t rowb = static_cast<uint32_t>(g.K) * 2u;
+    for (int a = r0; a < r1 && !stop; a += g.RT) {
+      const int nr = min(g.RT, r1 - a);
+      int slot;
+      unsigned char *dst = claim(slot);
+      if (!dst) return;
+      const uint16_t *src[3];
+      uint32_t bytes[3];
+      int n = 0;
+      if (kind == GV_QKV) {
+        const int qr = p.Hq * p.d, kr = p.Hkv * p.d;
+        const int segs[4] = {0, qr, qr + kr, qr + 2 * kr};
+        const uint16_t *mats[3] = {p.layers[layer].wq, p.layers[layer].wk, p.layers[layer].wv};
+        for (int s = 0; s < 3; ++s) {
+          const int lo = max(a, segs[s]), hi = min(a + nr, segs[s + 1]);
+          if (lo < hi) {
+            src[n] = mats[s] + static_cast<size_t>(lo - segs[s]) * g.K;
+            bytes[n] = static_cast<uint32_t>(hi - lo) * rowb;
+            ++n;
+          }
+        }
+      } else if (kind == GV_GU) {
+        src[0] = p.layers[layer].w_gate + static_cast<size_t>(a) * g.K;
+        src[1] = p.layers[layer].w_up + static_cast<size_t>(a) * g.K;
+        bytes[0] = bytes[1] = static_cast<uint32_t>(nr) * rowb;
+        n = 2;
+      } else {
+        const uint16_t *base = kind == GV_O ? p.layers[layer].wo
+                             : kind == GV_DOWN ? p.layers[layer].w_down
+                                               : p.lm_head;
+        src[0] = base + static_cast<size_t>(a) * g.K;
+        bytes[0] = static_cast<uint32_t>(nr) * rowb;
+        n = 1;
+      }
+      uint32_t total = 0;
+      for (int i = 0; i < n; ++i) total += bytes[i];
+      mbar_arrive_expect_tx(&S.full[slot], total);
+      uint32_t off = 0;
+      for (int i = 0; i < n; ++i) {
+        bulk_load(dst + off, src[i], bytes[i], &S.full[slot], pol_w);
+        off += bytes[i];
+      }
+      ++it;
+    }
+  }
+
+  template <int HD>
+  __device__ void kv_tiles(int l, int f, int cta) {
+    const AttnSched as = attn_sched(p, f);
+    const int TP = p.stage_bytes / (4 * HD);
+    bool guarded = false;
+    for (int u = cta; u < as.units && !stop; u += p.G) {
+      const int g = u / as.C, c = u % as.C;
+      const int a = c * as.cs, b = min(a + as.cs, as.ctx);
+      const int pend = min(b, as.P);
+      for (int p0 = a; p0 < pend && !stop; p0 += TP) {
+        if (!guarded) {
+          // position P-1 was appended by this launch's previous forward: wait
+          // until this CTA's consumers have passed that attention phase
+          const int need = (f - 1) * p.L + l + 1;
+          if (f > 0) {
+            Deadline dl;
+            int n = 0;
+            while (ld_acquire_cta(&S.flags[F_ATTN_DONE]) < need) {
+              if ((++n & 63) == 0) {
+                if (flag(S, F_ABORT)) { stop = true; return; }
+                if (dl.expired(p.spin_ns)) { set_err(p, MK_ERR_TIMEOUT_D); stop = true; return; }
+              }
+            }
+          }
+          fence_proxy_async_global();
+          guarded = true;
+        }
+        const int np = min(TP, pend - p0);
+        int slot;
+        unsigned char *dst = claim(slot);
+        if (!dst) return;
+        const size_t row0 = (static_cast<size_t>(l) * p.Hkv + g) * p.max_seq + p0;
+        const uint32_t bytes = static_cast<uint32_t>(np) * HD * 2u;
+        mbar_arrive_expect_tx(&S.full[slot], 2u * bytes);
+        bulk_load(dst, p.kcache + row0 * HD, bytes, &S.full[slot], pol_kv);
+        bulk_load(dst + bytes, p.vcache + row0 * HD, bytes, &S.full[slot], pol_kv);
+        ++it;
+      }
+    }
+  }
+
+  // wait for every copy this producer issued (each slot's latest fill)
+  __device__ void drain() {
+    const uint32_t ns = static_cast<uint32_t>(p.stages);
+    const uint32_t used = it < ns ? it : ns;
+    for (uint32_t s = 0; s < used; ++s) {
+      const uint32_t last = ((it - 1 - s) / ns) * ns + s;     // largest fill index of slot s
+      const uint32_t par = (last / ns) & 1u;
+      Deadline dl;
+      int n = 0;
+      while (!mbar_try_wait(&S.full[s], par)) {
+        if ((++n & 63) == 0 && dl.expired(p.spin_ns)) { set_err(p, MK_ERR_TIMEOUT_D); break; }
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <int HD>
+__global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  SmemCtl &S = *reinterpret_cast<SmemCtl *>(smem_raw);
+  unsigned char *ring = smem_raw + RING_OFFSET;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cta = blockIdx.x;
+  const int NPH = 5 * p.L + 1;
+
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], NCW);
+    }
+    fence_mbar_init();
+    flag(S, F_ABORT) = (p.per_op && ld_relaxed_i32(p.err) != 0) ? 1 : 0;
+    flag(S, F_PROD_DONE) = 0;
+    flag(S, F_ATTN_DONE) = p.per_op ? INT_MAX : 0;
+    flag(S, F_LAST) = 0;
+  }
+  __syncthreads();
+  if (flag(S, F_ABORT)) return;   // per-op launch after an earlier failure: nothing runs
+
+  int gp_begin, gp_end;
+  bool final_select;
+  if (p.per_op) {
+    if (p.op_phase >= NPH) { gp_begin = gp_end = 0; final_select = true; }
+    else { gp_begin = p.op_fwd * NPH + p.op_phase; gp_end = gp_begin + 1; final_select = false; }
+  } else {
+    gp_begin = 0;
+    gp_end = p.n_fwd * NPH;
+    final_select = true;
+  }
+
+  if (warp == NCW) {
+    // ---------------- producer warp (lane 0 issues everything) ----------------
+    if (lane == 0) {
+      Producer pr(p, S, ring);
+      for (int gp = gp_begin; gp < gp_end && !pr.stop; ++gp) {
+        const int f = gp / NPH, ph = gp % NPH;
+        if (ph == 5 * p.L) { pr.gemv_tiles(GV_LM, 0, cta); continue; }
+        const int l = ph / 5;
+        switch (ph % 5) {
+          case 0: pr.gemv_tiles(GV_QKV, l, cta); break;
+          case 1: pr.kv_tiles<HD>(l, f, cta); break;
+          case 2: pr.gemv_tiles(GV_O, l, cta); break;
+          case 3: pr.gemv_tiles(GV_GU, l, cta); break;
+          default: pr.gemv_tiles(GV_DOWN, l, cta); break;
+        }
+      }
+      pr.drain();
+      st_release_cta(&S.flags[F_PROD_DONE], 1);
+    }
+    return;
+  }
+
+  // -------------------------- consumer warps ----------------------------------
+  uint32_t it = 0;
+  int rb = 0;
+  unsigned bar_target = 0;
+  int bar_index = 0;
+  int in_id = 0;
+  bool ok = true;
+  for (int gp = gp_begin; gp < gp_end && ok; ++gp) {
+    const int f = gp / NPH, ph = gp % NPH;
+    if (ph == 5 * p.L) {
+      gemv_dispatch(p, S, ring, GV_LM, 0, f, cta, in_id, it, rb);
+    } else {
+      const int l = ph / 5, k = ph % 5;
+      if (k == 0 && l == 0) {
+        // the token of this forward: teacher-forced input, or fed back in-kernel
+        int prev = 0;
+        if (f > 0) prev = select_token(p, S, f - 1, cta, false);
+        int id;
+        if (f < p.n_in) id = p.in_ids[f];
+        else if (f > 0) id = prev;
+        else id = *p.last_id;
+        const bool bad = (id >= 0) ? (id >= p.vocab_in)
+                                   : (p.embeds == nullptr || -(id + 1) >= p.n_embed_rows);
+        if (bad) {
+          if (tid == 0) set_err(p, MK_ERR_BAD_TOKEN_D);
+          ok = false;
+          break;
+        }
+        in_id = id;
+      }
+      switch (k) {
+        case 0: gemv_dispatch(p, S, ring, GV_QKV, l, f, cta, in_id, it, rb); break;
+        case 1: attention_dispatch<HD>(p, S, ring, l, f, cta, it); break;
+        case 2: gemv_dispatch(p, S, ring, GV_O, l, f, cta, in_id, it, rb); break;
+        case 3: gemv_dispatch(p, S, ring, GV_GU, l, f, cta, in_id, it, rb); break;
+        default: gemv_dispatch(p, S, ring, GV_DOWN, l, f, cta, in_id, it, rb); break;
+      }
+    }
+    if (!p.per_op) {
+      ok = grid_barrier(p, S, bar_target, bar_index++, cta);
+      if (tid == 0) {
+        if (p.trace) p.trace[static_cast<size_t>(gp) * p.G + cta] = globaltimer();
+        if (ph < 5 * p.L && ph % 5 == 1) st_release_cta(&S.flags[F_ATTN_DONE], f * p.L + ph / 5 + 1);
+      }
+    } else {
+      cons_sync();
+      ok = flag(S, F_ABORT) == 0;
+    }
+  }
+  if (ok && final_select && flag(S, F_ABORT) == 0) select_token(p, S, p.n_fwd - 1, cta, true);
+
+  // ---- shutdown: stop the producer and wait until its copies have landed ----
+  cons_sync();
+  if (tid == 0) {
+    flag(S, F_ABORT) = 1;
+    Deadline dl;
+    int n = 0;
+    while (ld_acquire_cta(&S.flags[F_PROD_DONE]) == 0) {
+      if ((++n & 255) == 0 && dl.expired(2 * p.spin_ns)) { set_err(p, MK_ERR_TIMEOUT_D); break; }
+    }
+  }
+  cons_sync();
+}
+
+}  // namespace mk

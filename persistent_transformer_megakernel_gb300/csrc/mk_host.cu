@@ -1,0 +1,423 @@
+// Host side of libmk.so: the C ABI declared in include/mk.h.
+//
+// mk_create validates the shape, fixes the GEMV thread geometry of every phase,
+// allocates the KV cache and scratch, builds the rotary cos/sin table on the
+// host in double precision ("RoPE freq? Python tables only", page B = "I made a
+// single CUDA kernel speak: streaming Qwen3-TTS at 50ms latency on an RTX 5090",
+// section "So, What's the Catch with These Megakernels?") and checks that one
+// CTA per SM fits.  mk_decode runs all forwards of a call in one cooperative
+// launch (page A = "Porting a 1,200-line persistent CUDA megakernel to
+// Qwen3-TTS", section "The idea: one kernel that never exits"), or, with
+// MK_DECODE_PER_OP, one ordinary launch per phase.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/mk.h"
+#include "mk_launch.h"
+#include "mk_params.h"
+
+namespace {
+
+constexpr int kStageBytes = 32 * 1024;
+constexpr int kStages = 6;
+constexpr int kMinChunks = 64;   // split-KV chunk capacity per kv head (at least grid / Hkv)
+
+struct DeviceBuffers {
+  std::vector<void *> owned;
+  int alloc(void **p, size_t bytes) {
+    if (bytes == 0) bytes = 16;
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      *p = nullptr;
+      return e == cudaErrorMemoryAllocation ? MK_ERR_NO_MEMORY : MK_ERR_CUDA;
+    }
+    owned.push_back(*p);
+    return MK_OK;
+  }
+  void free_all() {
+    for (void *p : owned) cudaFree(p);
+    owned.clear();
+  }
+};
+
+int choose_kpt(int K, int &kpt, int &tpr) {
+  static const int kpts[] = {8, 12, 16, 24};
+  for (int c : kpts) {
+    if (K % c) continue;
+    const int t = K / c;
+    if (t == 32 || t == 64 || t == 128 || t == 256) {
+      kpt = c;
+      tpr = t;
+      return MK_OK;
+    }
+  }
+  return MK_ERR_UNSUPPORTED;
+}
+
+int pow2_at_least(int v) {
+  int p = 1;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+// thread geometry of one GEMV phase: K input width, rows (pairs for gate/up)
+int make_geom(int K, int rows, bool pairs, mk::GemvGeom &g) {
+  int kpt, tpr;
+  if (choose_kpt(K, kpt, tpr) != MK_OK) return MK_ERR_UNSUPPORTED;
+  g.K = K;
+  g.KPT = kpt;
+  g.TPR = tpr;
+  g.NG = mk::NCT / tpr;
+  const int rows_fit = kStageBytes / (K * 2);
+  if (pairs) {
+    g.RT = std::min(rows_fit / 2, 8 * g.NG);
+    if (g.RT < 1) return MK_ERR_UNSUPPORTED;
+    g.RPTP = pow2_at_least((2 * g.RT + g.NG - 1) / g.NG);
+  } else {
+    g.RT = std::min(rows_fit, 16 * g.NG);
+    if (g.RT < 1) return MK_ERR_UNSUPPORTED;
+    g.RPTP = pow2_at_least((g.RT + g.NG - 1) / g.NG);
+  }
+  if (g.RPTP > 16) return MK_ERR_UNSUPPORTED;
+  g.rows = rows;
+  return MK_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct mk_handle {
+  mk_config cfg;
+  int device = 0;
+  int G = 0;
+  int smem = 0;
+  int pos = 0;
+  int max_chunks = 0;
+  int64_t weight_bytes = 0, kv_bytes = 0;
+  const void *kernel = nullptr;
+  DeviceBuffers buf;
+  mk::Params base;      // call-independent launch parameters
+  int *d_sync = nullptr;       // [0] barrier counter, [1] error word, [2] last id
+  int32_t *d_ids_in = nullptr, *d_ids_out = nullptr;
+};
+
+extern "C" {
+
+const char *mk_error_string(int code) {
+  switch (code) {
+    case MK_OK: return "ok";
+    case MK_ERR_INVALID_ARG: return "invalid argument";
+    case MK_ERR_UNSUPPORTED: return "unsupported shape or launch geometry";
+    case MK_ERR_KV_FULL: return "KV cache full";
+    case MK_ERR_BAD_TOKEN: return "token id or sentinel row out of range";
+    case MK_ERR_TIMEOUT: return "device wait timed out";
+    case MK_ERR_NUMERIC: return "non-finite logit";
+    case MK_ERR_CUDA: return "CUDA runtime error";
+    case MK_ERR_NO_MEMORY: return "device out of memory";
+    case MK_ERR_BAD_POSITION: return "position stream outside the rotary table";
+    default: return "unknown error";
+  }
+}
+
+int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
+  if (!cfg || !w || !out) return MK_ERR_INVALID_ARG;
+  *out = nullptr;
+  const mk_config c = *cfg;
+  if (c.n_layers < 1 || c.hidden < 1 || c.n_q_heads < 1 || c.n_kv_heads < 1 || c.head_dim < 1 ||
+      c.intermediate < 1 || c.vocab < 1 || c.vocab_in < 1 || c.max_seq < 1 || c.rope_positions < 0 ||
+      !(c.rms_eps >= 0.f) || !(c.rope_theta > 0.f) || c.flags != 0)
+    return MK_ERR_INVALID_ARG;
+  if (c.head_dim != 64 && c.head_dim != 128) return MK_ERR_UNSUPPORTED;
+  if (c.n_q_heads % c.n_kv_heads) return MK_ERR_UNSUPPORTED;
+  const int grp = c.n_q_heads / c.n_kv_heads;
+  if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return MK_ERR_UNSUPPORTED;
+  if (grp * c.head_dim > mk::MAX_GRP_HD) return MK_ERR_UNSUPPORTED;
+  if (c.rope_mode != 0 && c.rope_mode != 1) return MK_ERR_INVALID_ARG;
+  if (c.rope_mode == 1) {
+    if (c.mrope_sections[0] < 0 || c.mrope_sections[1] < 0 || c.mrope_sections[2] < 0 ||
+        c.mrope_sections[0] + c.mrope_sections[1] + c.mrope_sections[2] != c.head_dim / 2)
+      return MK_ERR_INVALID_ARG;
+  }
+  if (!w->embed || !w->final_norm || !w->layers) return MK_ERR_INVALID_ARG;
+  if (!w->lm_head && c.vocab != c.vocab_in) return MK_ERR_INVALID_ARG;
+  if (!aligned16(w->embed) || !aligned16(w->final_norm) || (w->lm_head && !aligned16(w->lm_head)))
+    return MK_ERR_INVALID_ARG;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const mk_layer_weights &L = w->layers[l];
+    const void *ps[] = {L.attn_norm, L.wq, L.wk, L.wv, L.q_norm, L.k_norm, L.wo, L.mlp_norm, L.w_gate, L.w_up, L.w_down};
+    for (const void *q : ps)
+      if (!q || !aligned16(q)) return MK_ERR_INVALID_ARG;
+  }
+  const int H = c.hidden, d = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads, I = c.intermediate;
+
+  mk::GemvGeom geo[mk::GV_COUNT];
+  if (make_geom(H, (Hq + 2 * Hkv) * d, false, geo[mk::GV_QKV]) ||
+      make_geom(Hq * d, H, false, geo[mk::GV_O]) ||
+      make_geom(H, I, true, geo[mk::GV_GU]) ||
+      make_geom(I, H, false, geo[mk::GV_DOWN]) ||
+      make_geom(H, c.vocab, false, geo[mk::GV_LM]))
+    return MK_ERR_UNSUPPORTED;
+
+  mk_handle *h = new (std::nothrow) mk_handle();
+  if (!h) return MK_ERR_NO_MEMORY;
+  h->cfg = c;
+  int rc = MK_OK;
+  auto fail = [&](int code) {
+    h->buf.free_all();
+    delete h;
+    return code;
+  };
+  if (cudaGetDevice(&h->device) != cudaSuccess) return fail(MK_ERR_CUDA);
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, h->device) != cudaSuccess) return fail(MK_ERR_CUDA);
+  int coop = 0;
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device);
+  if (!coop) return fail(MK_ERR_UNSUPPORTED);
+  h->G = prop.multiProcessorCount;
+  h->kernel = (d == 64) ? mk::kernel_d64() : mk::kernel_d128();
+  h->smem = mk::RING_OFFSET + kStages * kStageBytes;
+  if (h->smem > static_cast<int>(prop.sharedMemPerBlockOptin)) return fail(MK_ERR_UNSUPPORTED);
+  if (cudaFuncSetAttribute(h->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, h->smem) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(MK_ERR_CUDA);
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, h->kernel, mk::NTHREADS, h->smem) != cudaSuccess ||
+      per_sm < 1) {
+    cudaGetLastError();
+    return fail(MK_ERR_UNSUPPORTED);
+  }
+  h->max_chunks = std::max(kMinChunks, h->G / Hkv);
+
+  // ---- allocations ---------------------------------------------------------
+  const int rope_len = c.rope_positions > 0 ? c.rope_positions : 2 * c.max_seq + 8;
+  const size_t kv_elems = static_cast<size_t>(c.n_layers) * Hkv * c.max_seq * d;
+  mk::LayerPtrs *d_layers = nullptr;
+  uint16_t *kc = nullptr, *vc = nullptr;
+  float2 *rope = nullptr;
+  float *x = nullptr, *qkv = nullptr, *attn = nullptr, *u = nullptr, *part = nullptr, *cand_val = nullptr;
+  int *cand_idx = nullptr;
+  unsigned *tickets = nullptr;
+  if ((rc = h->buf.alloc((void **)&d_layers, sizeof(mk::LayerPtrs) * c.n_layers)) ||
+      (rc = h->buf.alloc((void **)&kc, kv_elems * 2)) ||
+      (rc = h->buf.alloc((void **)&vc, kv_elems * 2)) ||
+      (rc = h->buf.alloc((void **)&rope, sizeof(float2) * static_cast<size_t>(rope_len) * (d / 2))) ||
+      (rc = h->buf.alloc((void **)&x, sizeof(float) * H)) ||
+      (rc = h->buf.alloc((void **)&qkv, sizeof(float) * (Hq + 2 * Hkv) * d)) ||
+      (rc = h->buf.alloc((void **)&attn, sizeof(float) * Hq * d)) ||
+      (rc = h->buf.alloc((void **)&u, sizeof(float) * I)) ||
+      (rc = h->buf.alloc((void **)&part, sizeof(float) * static_cast<size_t>(Hq) * h->max_chunks * (d + 2))) ||
+      (rc = h->buf.alloc((void **)&cand_val, sizeof(float) * h->G)) ||
+      (rc = h->buf.alloc((void **)&cand_idx, sizeof(int) * h->G)) ||
+      (rc = h->buf.alloc((void **)&tickets, sizeof(unsigned) * Hkv)) ||
+      (rc = h->buf.alloc((void **)&h->d_sync, sizeof(int) * 4)) ||
+      (rc = h->buf.alloc((void **)&h->d_ids_in, sizeof(int32_t) * c.max_seq)) ||
+      (rc = h->buf.alloc((void **)&h->d_ids_out, sizeof(int32_t) * c.max_seq)))
+    return fail(rc);
+
+  std::vector<mk::LayerPtrs> lp(c.n_layers);
+  for (int l = 0; l < c.n_layers; ++l) {
+    const mk_layer_weights &L = w->layers[l];
+    lp[l] = mk::LayerPtrs{(const uint16_t *)L.attn_norm, (const uint16_t *)L.wq, (const uint16_t *)L.wk,
+                          (const uint16_t *)L.wv, (const uint16_t *)L.q_norm, (const uint16_t *)L.k_norm,
+                          (const uint16_t *)L.wo, (const uint16_t *)L.mlp_norm, (const uint16_t *)L.w_gate,
+                          (const uint16_t *)L.w_up, (const uint16_t *)L.w_down};
+  }
+  // rotary table: cos/sin(pos * theta^(-2i/d)) evaluated in double
+  std::vector<float2> tab(static_cast<size_t>(rope_len) * (d / 2));
+  for (int pos = 0; pos < rope_len; ++pos)
+    for (int i = 0; i < d / 2; ++i) {
+      const double omega = std::pow(static_cast<double>(c.rope_theta), -2.0 * i / d);
+      const double phi = pos * omega;
+      tab[static_cast<size_t>(pos) * (d / 2) + i] = make_float2(static_cast<float>(std::cos(phi)),
+                                                                static_cast<float>(std::sin(phi)));
+    }
+  if (cudaMemcpy(d_layers, lp.data(), sizeof(mk::LayerPtrs) * c.n_layers, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(rope, tab.data(), sizeof(float2) * tab.size(), cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemset(tickets, 0, sizeof(unsigned) * Hkv) != cudaSuccess ||
+      cudaMemset(h->d_sync, 0, sizeof(int) * 4) != cudaSuccess ||
+      cudaMemset(kc, 0, kv_elems * 2) != cudaSuccess || cudaMemset(vc, 0, kv_elems * 2) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return fail(MK_ERR_CUDA);
+  }
+
+  mk::Params &p = h->base;
+  std::memset(&p, 0, sizeof(p));
+  p.L = c.n_layers; p.H = H; p.Hq = Hq; p.Hkv = Hkv; p.d = d; p.I = I; p.V = c.vocab; p.vocab_in = c.vocab_in;
+  p.grp = grp;
+  p.eps = c.rms_eps;
+  p.inv_sqrt_d = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+  p.rope_mode = c.rope_mode;
+  p.sec_b0 = c.rope_mode ? c.mrope_sections[0] : d / 2;
+  p.sec_b1 = c.rope_mode ? c.mrope_sections[0] + c.mrope_sections[1] : d / 2;
+  p.max_seq = c.max_seq;
+  p.rope_len = rope_len;
+  p.max_chunks = h->max_chunks;
+  p.layers = d_layers;
+  p.embed = (const uint16_t *)w->embed;
+  p.lm_head = (const uint16_t *)(w->lm_head ? w->lm_head : w->embed);
+  p.final_norm = (const uint16_t *)w->final_norm;
+  p.kcache = kc; p.vcache = vc; p.rope = rope;
+  p.x = x; p.qkv = qkv; p.attn = attn; p.u = u; p.part = part;
+  p.cand_val = cand_val; p.cand_idx = cand_idx; p.tickets = tickets;
+  p.bar = reinterpret_cast<unsigned *>(h->d_sync);
+  p.err = h->d_sync + 1;
+  p.last_id = h->d_sync + 2;
+  p.G = h->G;
+  p.stages = kStages;
+  p.stage_bytes = kStageBytes;
+  for (int k = 0; k < mk::GV_COUNT; ++k) p.geo[k] = geo[k];
+
+  const int64_t layer_params = static_cast<int64_t>(H) * (Hq + 2 * Hkv) * d + static_cast<int64_t>(Hq) * d * H +
+                               3LL * H * I + 2LL * H + 2LL * d;
+  h->weight_bytes = 2 * (layer_params * c.n_layers + static_cast<int64_t>(c.vocab) * H + H);
+  h->kv_bytes = static_cast<int64_t>(kv_elems) * 4;
+  *out = h;
+  return MK_OK;
+}
+
+int mk_reset_kv(mk_handle *h, mk_stream stream) {
+  if (!h) return MK_ERR_INVALID_ARG;
+  h->pos = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(h->d_sync, 0, sizeof(int) * 4, s) != cudaSuccess ||
+      cudaMemsetAsync(h->base.tickets, 0, sizeof(unsigned) * h->cfg.n_kv_heads, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
+  return MK_OK;
+}
+
+int mk_decode(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_steps, int32_t *d_out_ids,
+              const mk_decode_opts *opts, mk_stream stream) {
+  if (!h || n_in < 0 || n_steps < 0) return MK_ERR_INVALID_ARG;
+  const int n_fwd = n_in + n_steps;
+  if (n_fwd == 0) return MK_OK;
+  if (!d_out_ids || (n_in > 0 && !d_in_ids)) return MK_ERR_INVALID_ARG;
+  mk_decode_opts o;
+  std::memset(&o, 0, sizeof(o));
+  o.fault_skip_barrier = -1;
+  if (opts) o = *opts;
+  if (o.n_embed_rows < 0 || o.attn_chunks < 0 || o.attn_chunks > h->max_chunks || o.spin_ns < 0 ||
+      (o.flags & ~MK_DECODE_PER_OP) || (o.n_embed_rows > 0 && !o.embeds))
+    return MK_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(h->pos) + n_fwd > h->cfg.max_seq) return MK_ERR_KV_FULL;
+  if (cudaSetDevice(h->device) != cudaSuccess) return MK_ERR_CUDA;
+
+  mk::Params p = h->base;
+  p.in_ids = d_in_ids;
+  p.n_in = n_in;
+  p.n_fwd = n_fwd;
+  p.pos0 = h->pos;
+  p.out_ids = d_out_ids;
+  p.embeds = o.embeds;
+  p.n_embed_rows = o.embeds ? o.n_embed_rows : 0;
+  p.pos3 = o.pos3;
+  p.logits = o.logits;
+  p.hidden = o.hidden;
+  p.trace = reinterpret_cast<unsigned long long *>(o.trace);
+  p.chunks_override = o.attn_chunks;
+  p.spin_ns = o.spin_ns > 0 ? o.spin_ns : 1000000000LL;
+  p.fault_barrier = o.fault_skip_barrier;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // barrier counter, error word and merge tickets start at zero for every call
+  if (cudaMemsetAsync(h->d_sync, 0, sizeof(int) * 2, s) != cudaSuccess ||
+      cudaMemsetAsync(h->base.tickets, 0, sizeof(unsigned) * h->cfg.n_kv_heads, s) != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
+  cudaError_t e = cudaSuccess;
+  if (!(o.flags & MK_DECODE_PER_OP)) {
+    p.per_op = 0;
+    void *args[] = {&p};
+    e = cudaLaunchCooperativeKernel(h->kernel, dim3(h->G), dim3(mk::NTHREADS), args, h->smem, s);
+  } else {
+    // the launch-overhead ablation: the same phases, one ordinary launch each
+    p.per_op = 1;
+    p.fault_barrier = -1;
+    const int nph = 5 * p.L + 1;
+    void *args[] = {&p};
+    for (int f = 0; f < n_fwd && e == cudaSuccess; ++f)
+      for (int ph = 0; ph < nph && e == cudaSuccess; ++ph) {
+        p.op_fwd = f;
+        p.op_phase = ph;
+        e = cudaLaunchKernel(h->kernel, dim3(h->G), dim3(mk::NTHREADS), args, h->smem, s);
+      }
+    if (e == cudaSuccess) {
+      p.op_fwd = n_fwd;
+      p.op_phase = nph;      // final greedy selection
+      e = cudaLaunchKernel(h->kernel, dim3(h->G), dim3(mk::NTHREADS), args, h->smem, s);
+    }
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
+  int herr = 0;
+  if (cudaMemcpyAsync(&herr, h->d_sync + 1, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
+  if (herr != 0) return herr;
+  h->pos += n_fwd;
+  return MK_OK;
+}
+
+int mk_decode_host(mk_handle *h, const int32_t *h_in_ids, int32_t n_in, int32_t n_steps, int32_t *h_out_ids,
+                   const mk_decode_opts *opts, mk_stream stream) {
+  if (!h || n_in < 0 || n_steps < 0 || !h_out_ids || (n_in > 0 && !h_in_ids)) return MK_ERR_INVALID_ARG;
+  const int n_fwd = n_in + n_steps;
+  if (n_fwd > h->cfg.max_seq) return MK_ERR_KV_FULL;
+  if (n_fwd == 0) return MK_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaSetDevice(h->device) != cudaSuccess) return MK_ERR_CUDA;
+  if (n_in > 0 &&
+      cudaMemcpyAsync(h->d_ids_in, h_in_ids, sizeof(int32_t) * n_in, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
+  const int rc = mk_decode(h, h->d_ids_in, n_in, n_steps, h->d_ids_out, opts, stream);
+  if (rc != MK_OK) return rc;
+  if (cudaMemcpyAsync(h_out_ids, h->d_ids_out, sizeof(int32_t) * n_fwd, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
+  return MK_OK;
+}
+
+int mk_get_info(const mk_handle *h, mk_info *info) {
+  if (!h || !info) return MK_ERR_INVALID_ARG;
+  info->grid = h->G;
+  info->threads = mk::NTHREADS;
+  info->stages = kStages;
+  info->stage_bytes = kStageBytes;
+  info->smem_bytes = h->smem;
+  info->position = h->pos;
+  info->max_chunks = h->max_chunks;
+  info->weight_bytes = h->weight_bytes;
+  info->kv_bytes = h->kv_bytes;
+  return MK_OK;
+}
+
+int mk_destroy(mk_handle *h) {
+  if (!h) return MK_OK;
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  h->buf.free_all();
+  delete h;
+  return MK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,96 @@
+// Launch parameters shared by the host library and the device code.
+#pragma once
+#include <cstdint>
+
+namespace mk {
+
+constexpr int NCW = 8;               // consumer warps per CTA
+constexpr int NCT = NCW * 32;        // consumer threads
+constexpr int NTHREADS = NCT + 32;   // + one TMA producer warp
+constexpr int MAX_STAGES = 8;
+
+// GEMV phases in the order of their geometry table
+enum GemvKind { GV_QKV = 0, GV_O = 1, GV_GU = 2, GV_DOWN = 3, GV_LM = 4, GV_COUNT = 5 };
+
+// how a GEMV phase maps rows and the input width onto the consumer threads:
+// thread t owns KPT consecutive input elements (k-chunk t % TPR) of NG = 256/TPR
+// row groups; a tile holds RT rows (GU: RT gate/up row pairs).
+struct GemvGeom {
+  int K;        // input width
+  int KPT;      // input elements per thread (8, 12, 16, 24)
+  int TPR;      // threads per row (32, 64, 128, 256)
+  int NG;       // row groups = 256 / TPR
+  int RT;       // rows (pairs for GU) per ring tile
+  int RPTP;     // rows per thread per tile, padded to a power of two (<= 16)
+  int rows;     // total rows (pairs for GU) of the phase
+};
+
+struct LayerPtrs {
+  const uint16_t *attn_norm, *wq, *wk, *wv, *q_norm, *k_norm, *wo;
+  const uint16_t *mlp_norm, *w_gate, *w_up, *w_down;
+};
+
+struct Params {
+  // shape
+  int L, H, Hq, Hkv, d, I, V, vocab_in, grp;
+  float eps, inv_sqrt_d;
+  int rope_mode, sec_b0, sec_b1;   // pair i < sec_b0 -> stream 0, < sec_b1 -> 1, else 2
+  int max_seq, rope_len, max_chunks;
+  // weights (borrowed)
+  const LayerPtrs *layers;
+  const uint16_t *embed, *lm_head, *final_norm;
+  // handle-owned state and scratch
+  uint16_t *kcache, *vcache;       // [L][Hkv][max_seq][d]
+  const float2 *rope;              // [rope_len][d/2] (cos, sin)
+  float *x, *qkv, *attn, *u, *part, *cand_val;
+  int *cand_idx;
+  unsigned *tickets;               // [Hkv]
+  unsigned *bar;                   // grid-barrier counter (zeroed before each launch)
+  int *err;                        // first error code
+  int *last_id;
+  // this call
+  const int32_t *in_ids;
+  int n_in, n_fwd, pos0;
+  int32_t *out_ids;
+  const float *embeds;
+  int n_embed_rows;
+  const int32_t *pos3;
+  float *logits, *hidden;
+  unsigned long long *trace;
+  int chunks_override;
+  long long spin_ns;
+  int fault_barrier;
+  int G;                           // CTAs
+  int stages, stage_bytes;
+  // per-op path: one launch runs phase `op_phase` of forward `op_fwd`
+  int per_op, op_fwd, op_phase;
+  GemvGeom geo[GV_COUNT];
+};
+
+}  // namespace mk
+
+namespace mk {
+
+// flags shared inside a CTA between the consumer warps and the producer lane
+enum SmemFlag { F_ABORT = 0, F_PROD_DONE = 1, F_ATTN_DONE = 2, F_LAST = 3, F_TOKEN = 4, F_COUNT = 8 };
+
+constexpr int MAX_GRP_HD = 512;   // group size * head_dim handled by one attention unit
+
+// static part of the dynamic shared memory; the weight ring follows at RING_OFFSET
+struct SmemCtl {
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
+  float red[2][NCW][32];            // per-warp row partials, double buffered by tile
+  float misc[64];
+  int flags[F_COUNT];
+  float bestv[NCW];
+  int besti[NCW];
+  float qs[MAX_GRP_HD];             // normed, rotated, scaled queries of one unit
+  float kcur[128], vcur[128];       // this position's key / value (bf16-rounded)
+  float ow[NCW][MAX_GRP_HD];        // per-warp unnormalised attention outputs
+  float mw[NCW][8], lw[NCW][8];     // per-warp running max / sum per head
+};
+
+constexpr int RING_OFFSET = (int)((sizeof(SmemCtl) + 1023) / 1024 * 1024);
+
+}  // namespace mk

@@ -1,0 +1,189 @@
+"""Parity of the CUDA megakernel (through the C ABI) with the CPU oracle.
+
+Every case draws its inputs from ``workloads`` (seeded), runs the oracle on the
+CPU, then runs the library on cuda:0 in the launch configuration the bench
+uses (one CTA per SM, one cooperative launch per call) and compares logits,
+the layer-by-layer hidden states and the greedy ids.  Teacher-forced runs feed
+the oracle's own id stream so that one near-tie flip cannot make later
+forwards incomparable.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+from parity_util import assert_close, assert_ids, first_near_tie
+
+pytestmark = pytest.mark.gpu
+
+mk = pytest.importorskip("persistent_transformer_megakernel_gb300")
+
+
+def _run_gpu(dec, feed, n_steps=0, embeds=None, pos3=None, per_op=False, attn_chunks=0):
+    s = dec.shape
+    n = len(feed) + n_steps
+    logits = torch.full((n, s["vocab"]), float("nan"), dtype=torch.float32, device="cuda:0")
+    hidden = torch.full((n, s["n_layers"] + 1, s["hidden"]), float("nan"), dtype=torch.float32,
+                        device="cuda:0")
+    ids = dec.decode(feed, n_steps, logits=logits, hidden=hidden, embeds=embeds, pos3=pos3,
+                     per_op=per_op, attn_chunks=attn_chunks)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), logits.double().cpu().numpy(), hidden.double().cpu().numpy()
+
+
+def _teacher_forced(name, n_prompt, n_steps, max_seq=64, pos3_mode=None, per_op=False,
+                    attn_chunks=0):
+    s = W.shape(name)
+    w = W.make_weights(s, seed=0)
+    prompt = W.make_prompt(s["vocab_in"], n_prompt, seed=1)
+    n = n_prompt + n_steps
+    pos3 = None if pos3_mode is None else W.make_pos3(0, n, distinct=(pos3_mode == "distinct"))
+    ref = O.Decoder(s, w, max_seq=max_seq)
+    ids_ref, lg_ref, hd_ref = ref.generate(prompt, n_steps, pos3=pos3)
+    feed = np.concatenate([prompt, ids_ref[n_prompt - 1:n - 1]]).astype(np.int32)
+    dec = mk.Decoder(s, w, max_seq=max_seq)
+    p3 = None if pos3 is None else torch.as_tensor(pos3, device="cuda:0")
+    ids, lg, hd = _run_gpu(dec, feed, 0, pos3=p3, per_op=per_op, attn_chunks=attn_chunks)
+    assert_close(lg, lg_ref, name + " logits")
+    for l in range(s["n_layers"] + 1):
+        assert_close(hd[:, l], hd_ref[:, l], "%s hidden[%d]" % (name, l))
+    assert_ids(ids, ids_ref, lg_ref, name + " ids")
+    dec.close()
+    return ids, lg, hd
+
+
+@pytest.mark.parametrize("name,n_prompt,n_steps", [
+    ("tiny", 8, 16),          # the tiny oracle-check workload
+    ("mid", 5, 70),           # 0.6B-wide layers: several tiles per CTA, ragged vocab, 75 positions
+    ("gqa4", 6, 20),          # group 4, head_dim 64, tied head
+])
+def test_teacher_forced_parity(name, n_prompt, n_steps):
+    _teacher_forced(name, n_prompt, n_steps, max_seq=n_prompt + n_steps + 4)
+
+
+@pytest.mark.parametrize("mode", ["equal", "distinct"])
+def test_mrope_parity(mode):
+    _teacher_forced("mrope_small", 6, 10, max_seq=24, pos3_mode=mode)
+
+
+def test_free_running_greedy_matches_until_a_near_tie():
+    s = W.shape("tiny")
+    w = W.make_weights(s, seed=0)
+    prompt = W.make_prompt(s["vocab_in"], 8, seed=1)
+    ids_ref, lg_ref, _ = O.Decoder(s, w, max_seq=40).generate(prompt, 16)
+    dec = mk.Decoder(s, w, max_seq=40)
+    ids = dec.decode(prompt, 16).cpu().numpy()
+    k = first_near_tie(lg_ref)
+    assert np.array_equal(ids[:k], ids_ref[:k])
+    assert dec.position == 24
+
+
+def test_sentinel_rows_from_gpu_embed_sum():
+    # talker-style input: every forward is a negative id selecting a summed row
+    s = W.shape("mrope_small")
+    w = W.make_weights(s, seed=0)
+    n = 12
+    tables = W.make_tts_tables(s["hidden"], seed=3, codebook_size=256, text_vocab=1000)
+    codes, text = W.make_tts_codes(n, seed=2, codebook_size=256, text_vocab=1000)
+    E_ref = O.embed_sum17(tables["codebooks"], tables["text"], codes, text)
+    books = torch.from_numpy(tables["codebooks"].view(np.int16)).view(torch.bfloat16).cuda()
+    txt = torch.from_numpy(tables["text"].view(np.int16)).view(torch.bfloat16).cuda()
+    E = mk.embed_sum(books, txt, torch.as_tensor(codes).cuda(), torch.as_tensor(text).cuda())
+    torch.cuda.synchronize()
+    assert_close(E.double().cpu().numpy(), E_ref, "17-way embedding sum")
+    sid = W.sentinel_ids(n)
+    pos3 = W.make_pos3(0, n, distinct=True)
+    ids_ref, lg_ref, hd_ref = O.Decoder(s, w, max_seq=16).generate(sid, 0, sentinel_rows=E_ref, pos3=pos3)
+    dec = mk.Decoder(s, w, max_seq=16)
+    ids, lg, hd = _run_gpu(dec, sid, 0, embeds=E, pos3=torch.as_tensor(pos3, device="cuda:0"))
+    assert_close(lg, lg_ref, "sentinel logits")
+    assert_close(hd, hd_ref, "sentinel hidden")
+    assert_ids(ids, ids_ref, lg_ref)
+
+
+def test_per_op_path_is_bitwise_equal_to_persistent():
+    s = W.shape("mid")
+    w = W.make_weights(s, seed=0)
+    prompt = W.make_prompt(s["vocab_in"], 6, seed=1)
+    a = mk.Decoder(s, w, max_seq=32)
+    b = mk.Decoder(s, w, max_seq=32)
+    ia, la, ha = _run_gpu(a, prompt, 10)
+    ib, lb, hb = _run_gpu(b, prompt, 10, per_op=True)
+    assert np.array_equal(ia, ib) and np.array_equal(la, lb) and np.array_equal(ha, hb)
+
+
+def test_repeat_runs_are_deterministic_and_reset_works():
+    s = W.shape("mid")
+    w = W.make_weights(s, seed=0)
+    prompt = W.make_prompt(s["vocab_in"], 4, seed=1)
+    dec = mk.Decoder(s, w, max_seq=32)
+    i1, l1, h1 = _run_gpu(dec, prompt, 8)
+    dec.reset()
+    i2, l2, h2 = _run_gpu(dec, prompt, 8)
+    assert np.array_equal(i1, i2) and np.array_equal(l1, l2) and np.array_equal(h1, h2)
+
+
+@pytest.mark.parametrize("chunks", [1, 2, 7, 0, 64])
+def test_split_kv_result_independent_of_chunk_count(chunks):
+    s = W.shape("mid")
+    w = W.make_weights(s, seed=0)
+    prompt = W.make_prompt(s["vocab_in"], 40, seed=1)
+    ref = mk.Decoder(s, w, max_seq=48)
+    _, l_ref, h_ref = _run_gpu(ref, prompt, 0, attn_chunks=1)
+    dec = mk.Decoder(s, w, max_seq=48)
+    _, lg, hd = _run_gpu(dec, prompt, 0, attn_chunks=chunks)
+    assert np.abs(lg - l_ref).max() <= 1e-4 * max(1.0, np.abs(l_ref).max())
+    assert np.abs(hd - h_ref).max() <= 1e-4 * max(1.0, np.abs(h_ref).max())
+
+
+def test_calls_continue_from_the_cursor():
+    # one call of 10 forwards == a prompt call followed by a greedy-only call
+    s = W.shape("tiny")
+    w = W.make_weights(s, seed=0)
+    prompt = W.make_prompt(s["vocab_in"], 4, seed=1)
+    one = mk.Decoder(s, w, max_seq=16)
+    ia, la, _ = _run_gpu(one, prompt, 6)
+    two = mk.Decoder(s, w, max_seq=16)
+    ib1, lb1, _ = _run_gpu(two, prompt, 0)
+    ib2, lb2, _ = _run_gpu(two, [], 6)
+    assert np.array_equal(ia, np.concatenate([ib1, ib2]))
+    assert np.array_equal(la, np.concatenate([lb1, lb2]))
+    assert two.position == 10
+
+
+def test_host_buffer_entry_point_matches_device_one():
+    s = W.shape("tiny")
+    w = W.make_weights(s, seed=0)
+    prompt = W.make_prompt(s["vocab_in"], 5, seed=1)
+    a = mk.Decoder(s, w, max_seq=16)
+    b = mk.Decoder(s, w, max_seq=16)
+    ia = a.decode(prompt, 5).cpu().numpy()
+    ib = b.decode_host(prompt, 5)
+    assert np.array_equal(ia, ib)
+
+
+def test_errors_are_reported_not_raised_as_faults():
+    s = W.shape("tiny")
+    w = W.make_weights(s, seed=0)
+    dec = mk.Decoder(s, w, max_seq=8)
+    with pytest.raises(mk.MKError) as e:
+        dec.decode([3, s["vocab_in"] + 5], 0)                     # id beyond the table
+    assert e.value.code == -4
+    dec.reset()
+    with pytest.raises(mk.MKError) as e:
+        dec.decode([-1], 0)                                       # sentinel without a buffer
+    assert e.value.code == -4
+    dec.reset()
+    with pytest.raises(mk.MKError) as e:
+        dec.decode([1, 2, 3], 6)                                  # 9 forwards > max_seq 8
+    assert e.value.code == -3
+    dec.reset()
+    # a CTA that never arrives at a grid barrier: the others give up after the
+    # wait budget and the call returns a timeout instead of hanging
+    with pytest.raises(mk.MKError) as e:
+        dec.decode([1, 2], 0, spin_ns=20_000_000, fault_skip_barrier=3)
+    assert e.value.code == -5
+    dec.reset()
+    ids = dec.decode([1, 2], 2)                                   # the handle still works
+    assert ids.shape[0] == 4

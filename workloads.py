@@ -57,7 +57,7 @@ SHAPES = {
                 mrope_sections=None),
     # GQA group 4, head_dim 64, tied head, ragged vocab
     "gqa4": dict(n_layers=2, hidden=768, n_q_heads=8, n_kv_heads=2, head_dim=64,
-                 intermediate=1280, vocab=3001, vocab_in=3001, tied=True,
+                 intermediate=1536, vocab=3001, vocab_in=3001, tied=True,
                  mrope_sections=None),
     # talker-like MRoPE with head_dim 64 (sections of 32 pairs) and few layers
     "mrope_small": dict(n_layers=2, hidden=512, n_q_heads=8, n_kv_heads=4, head_dim=64,
