@@ -1,0 +1,392 @@
+"""Batch-1 decode benchmark of the persistent megakernel on GB300.
+
+Default workload: the Qwen3-0.6B-shaped decoder (28 layers, hidden 1024, 16/8
+heads, head_dim 128, MLP 3072, tied 151936 vocab), a 32-token random prompt
+and 512 greedy steps, seeded random-init bf16 weights.  One bench step =
+reset the KV cache, prefill the prompt (untimed, same kernel, one token per
+forward), then ONE persistent launch that runs the 512 greedy forwards; the
+CUDA events bracket that launch.  The weights (1.19 GB per forward) exceed
+the 129 MB L2, so no L2 flush is needed between steps.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the same workload instead.  Under torchrun every rank decodes its own replica
+on its own GPU (independent sessions, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def workload_desc(name):
+    wl = W.WORKLOADS[name]
+    s = W.shape(wl["shape"])
+    d = ("%s: %d layers, hidden %d, %d/%d heads, head_dim %d, MLP %d, vocab %d %s%s; "
+         "prompt %d + %d greedy steps" % (
+             name, s["n_layers"], s["hidden"], s["n_q_heads"], s["n_kv_heads"], s["head_dim"],
+             s["intermediate"], s["vocab"], "tied" if s["tied"] else "untied",
+             ", MRoPE %s" % (s["mrope_sections"],) if s["mrope_sections"] else "",
+             wl["prompt"], wl["steps"]))
+    return wl, s, d
+
+
+def algorithmic_bytes(s, weight_bytes, positions):
+    """Bytes one forward must move at slot P: all weights once, the KV cache
+    read for positions 0..P and the new K/V row written."""
+    kv_row = 2 * s["n_layers"] * s["n_kv_heads"] * s["head_dim"] * 2     # K and V, bf16
+    return sum(weight_bytes + kv_row * (P + 1) + kv_row for P in positions)
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", "mk_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reported baseline / the reference arm)
+# ---------------------------------------------------------------------------
+def cpu_oracle_rate(workload: str, n_forwards: int, threads: int, warmup: int = 0, steps: int = 1):
+    """Time the oracle in a child process with a fixed BLAS thread count: build
+    it once, run ``warmup`` untimed then ``steps`` timed samples of
+    ``n_forwards`` teacher-forced forwards.  Returns the seconds per sample."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(threads)
+    code = (
+        "import sys,time,json; sys.path.insert(0, %r)\n"
+        "import workloads as W, oracle as O\n"
+        "wl=W.WORKLOADS[%r]; s=W.shape(wl['shape']); w=W.make_weights(s, seed=0)\n"
+        "Wt=O.decoder.Weights(O.DecoderShape.from_dict(s), w); del w\n"
+        "n=%d; reps=%d+%d\n"
+        "dec=O.Decoder(s, None, max_seq=n*reps+2, weights=Wt)\n"
+        "p=W.make_prompt(s['vocab_in'], n*reps+1, seed=1)\n"
+        "dec.generate(p[:1], 0); out=[]\n"
+        "for r in range(reps):\n"
+        "    t=time.perf_counter(); dec.generate(p[1+r*n:1+(r+1)*n], 0); out.append(time.perf_counter()-t)\n"
+        "print(json.dumps(out[%d:]))\n" % (ROOT, workload, n_forwards, warmup, steps, warmup))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("oracle timing failed: " + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# the arms
+# ---------------------------------------------------------------------------
+def run_reference(args, rank, world):
+    """The oracle as it stands, timed on the host cores on bounded samples of
+    the same workload: each step is ``--cpu-forwards`` teacher-forced forwards."""
+    wl, s, desc = workload_desc(args.workload)
+    if rank != 0:
+        return
+    threads = cpu_threads()
+    n = max(1, args.cpu_forwards)
+    dts = cpu_oracle_rate(args.workload, n, threads, warmup=1, steps=args.steps)
+    total = sum(dts)
+    value = n * len(dts) / total
+    line = {
+        "impl": "reference", "metric": "batch-1 decode tok/s", "value": value, "unit": "tok/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / len(dts) * 1e3, "us_per_token": total / (n * len(dts)) * 1e6,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded random-init weights, random prompt ids)",
+        "config": {"workload": desc},
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": threads, "kind": "oracle",
+                         "sample": "%d teacher-forced forwards per step at context 2..%d, "
+                                   "float64 numpy oracle, BLAS threads %d" % (n, n * (args.steps + 1) + 1, threads)},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, rank, world):
+    import torch
+    import persistent_transformer_megakernel_gb300 as mk
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl, s, desc = workload_desc(args.workload)
+    n_prompt, n_steps = wl["prompt"], wl["steps"]
+    sentinel = wl.get("sentinel", False)
+
+    # CPU baseline before any heavy GPU work (rank 0 at N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        threads = cpu_threads()
+        n_cpu = max(1, args.cpu_forwards)
+        dts = cpu_oracle_rate(args.workload, n_cpu, threads, warmup=0, steps=1)
+        rate = n_cpu / dts[0]
+        cpu = {"value": rate, "unit": "tok/s", "cores": threads, "kind": "oracle",
+               "sample": "%d teacher-forced forwards of the same model at context 2..%d, "
+                         "float64 numpy oracle, BLAS threads %d" % (n_cpu, n_cpu + 1, threads)}
+
+    w = W.make_weights(s, seed=0)
+    max_seq = n_prompt + n_steps + 8
+    dec = mk.Decoder(s, w, max_seq=max_seq, device=dev)
+    del w
+    info = dec.info()
+    embeds = pos3 = None
+    if sentinel:
+        tables = W.make_tts_tables(s["hidden"], seed=3)
+        codes, text = W.make_tts_codes(n_prompt, seed=2)
+        books = torch.from_numpy(tables["codebooks"].view(np.int16)).view(torch.bfloat16).to(dev)
+        txt = torch.from_numpy(tables["text"].view(np.int16)).view(torch.bfloat16).to(dev)
+        embeds = mk.embed_sum(books, txt, torch.as_tensor(codes).to(dev), torch.as_tensor(text).to(dev))
+        del books, txt, tables
+        prompt = W.sentinel_ids(n_prompt)
+        pos3 = torch.as_tensor(W.make_pos3(0, n_prompt, distinct=True), device=dev)
+    else:
+        prompt = W.make_prompt(s["vocab_in"], n_prompt, seed=1)
+    d_prompt = torch.as_tensor(prompt, device=dev)
+    out = torch.empty(max_seq, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # the timed unit: greedy steps after the prompt; the talker workload times
+    # its sentinel forwards themselves (teacher-forced, no greedy tail)
+    if sentinel:
+        timed_positions = range(0, n_prompt)
+
+        def prep():
+            dec.reset()
+
+        def timed():
+            dec.decode(d_prompt, 0, out=out, embeds=embeds, pos3=pos3)
+        n_timed = n_prompt
+    else:
+        timed_positions = range(n_prompt, n_prompt + n_steps)
+
+        def prep():
+            dec.reset()
+            dec.decode(d_prompt, 0, out=out)
+
+        def timed():
+            dec.decode(None, n_steps, out=out)
+        n_timed = n_steps
+
+    for _ in range(args.warmup):
+        prep()
+        timed()
+    torch.cuda.synchronize()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    total_ms = 0.0
+    for _ in range(args.steps):
+        prep()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        timed()
+        e1.record(stream)
+        e1.synchronize()
+        total_ms += e0.elapsed_time(e1)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        dist.barrier()
+
+    tokens = n_timed * args.steps * world
+    value = tokens / (total_ms / 1e3)
+    per_launch_ms = total_ms / args.steps
+    bytes_launch = algorithmic_bytes(s, info["weight_bytes"], timed_positions)
+    peak, peak_src = load_peaks()
+    achieved = bytes_launch / (per_launch_ms / 1e3) / 1e9
+
+    # end to end through the C ABI with host id buffers (copies inside the region)
+    e2e_ms = 0.0
+    h_prompt = np.asarray(prompt, dtype=np.int32)
+    for i in range(args.steps + 1):
+        dec.reset()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        if sentinel:
+            dec.decode_host(h_prompt, 0, embeds=embeds, pos3=pos3)
+        else:
+            dec.decode_host(h_prompt, n_steps)
+        dt = (time.perf_counter() - t0) * 1e3
+        if i > 0:
+            e2e_ms += dt
+    e2e_tokens = (n_prompt + (0 if sentinel else n_steps)) * args.steps * world
+    e2e = {"value": e2e_tokens / (e2e_ms / 1e3), "unit": "tok/s",
+           "h2d_bytes_per_step": int(h_prompt.nbytes),
+           "d2h_bytes_per_step": int(4 * (n_prompt + (0 if sentinel else n_steps))),
+           "note": "mk_decode_host: prompt ids host->device, prompt + greedy forwards in one "
+                   "launch, all ids device->host; host wall clock"}
+
+    # launch-overhead ablation: the same phases as one ordinary launch each
+    ablation = None
+    if not args.no_ablation:
+        n_ab = min(args.ablation_forwards, n_timed)
+        dec.reset()
+        if not sentinel:
+            dec.decode(d_prompt, 0, out=out)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        if sentinel:
+            dec.decode(d_prompt[:n_ab], 0, out=out, embeds=embeds, pos3=pos3[:, :n_ab].contiguous(),
+                       per_op=True)
+        else:
+            dec.decode(None, n_ab, out=out, per_op=True)
+        e1.record(stream)
+        e1.synchronize()
+        ab_ms = e0.elapsed_time(e1)
+        ablation = {"us_per_token": ab_ms * 1e3 / n_ab, "forwards": n_ab,
+                    "launches_per_forward": 5 * s["n_layers"] + 1,
+                    "persistent_us_per_token": total_ms * 1e3 / (n_timed * args.steps)}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": "batch-1 decode tok/s",
+        "value": value,
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": per_launch_ms,
+        "us_per_token": total_ms * 1e3 / (n_timed * args.steps),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 weights / f32 compute",
+        "data": "synthetic (seeded random-init weights, random prompt ids)",
+        "config": {"workload": desc, "timed": "%d forwards per step in one persistent launch" % n_timed,
+                   "l2": "inputs larger than L2: %.2f GB of weights per forward" % (info["weight_bytes"] / 1e9),
+                   "grid": info["grid"], "threads": info["threads"],
+                   "ring": "%d x %d KB" % (info["stages"], info["stage_bytes"] // 1024),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": "%s hbm_gbs (copy bandwidth)" % peak_src,
+                     "algorithmic_bytes_per_launch": bytes_launch,
+                     "kernel": "mk::mk_decode_kernel<%d>" % s["head_dim"]},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if ablation is not None:
+        line["per_op_ablation"] = ablation
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
+    ap.add_argument("--workload", default="qwen3_0p6b", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--cpu-forwards", type=int, default=8)
+    ap.add_argument("--ablation-forwards", type=int, default=32)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-ablation", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and args.impl == "mk":
+        import torch
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world)
+    if world > 1 and args.impl == "mk":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -119,8 +119,9 @@ typedef struct {
   float *logits;              /* device [n_in + n_steps][vocab] fp32 out, or NULL */
   float *hidden;              /* device [n_in + n_steps][n_layers + 1][H] fp32 out, or NULL:
                                  the input row then the residual stream after each layer */
-  uint64_t *trace;            /* device [n_fwd][5*n_layers + 1][grid] %globaltimer stamps
-                                 taken after each phase's grid barrier, or NULL */
+  uint64_t *trace;            /* device [n_fwd][5*n_layers + 1][grid][4] %globaltimer stamps
+                                 of each CTA per phase: start, input in registers, tiles
+                                 done, grid barrier passed; or NULL */
   int32_t attn_chunks;        /* split-KV chunks per kv head; 0 = grid / n_kv_heads */
   int64_t spin_ns;            /* budget of every device wait; 0 = 1 s */
   int32_t fault_skip_barrier; /* test hook: CTA 0 skips its arrival at this grid barrier

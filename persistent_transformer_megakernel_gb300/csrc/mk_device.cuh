@@ -140,6 +140,12 @@ static __device__ bool grid_barrier(const Params &p, SmemCtl &S, unsigned &targe
   return flag(S, F_ABORT) == 0;
 }
 
+// optional %globaltimer stamps of thread 0: trace[((gp * G) + cta) * 4 + k],
+// k = 0 phase start, 1 input in registers, 2 tiles and epilogue done, 3 barrier passed
+__device__ __forceinline__ void trace_mark(const Params &p, int gp, int cta, int k) {
+  if (p.trace && threadIdx.x == 0) p.trace[(static_cast<size_t>(gp) * p.G + cta) * 4 + k] = globaltimer();
+}
+
 // ---------------------------------------------------------------------------
 // argmax helpers (largest value, lowest index among equals)
 // ---------------------------------------------------------------------------
@@ -255,7 +261,7 @@ __device__ __forceinline__ float input_elem(const Params &p, int id, int k) {
 // epilogue (store, residual add, SiLU*mul, logits + argmax candidate).
 template <int KPT, int RPTP>
 __device__ void gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer, int f,
-                           int cta, int in_id, uint32_t &it, int &rb) {
+                           int cta, int in_id, uint32_t &it, int &rb, int gp) {
   const GemvGeom g = p.geo[kind];
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int kc = t % g.TPR, rg = t / g.TPR;
@@ -288,6 +294,7 @@ __device__ void gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int
 #pragma unroll
     for (int j = 0; j < KPT; ++j) xr[j] = xr[j] * rs * bf2f(gain[k0 + j]);
   }
+  trace_mark(p, gp, cta, 1);
 
   // the first layer's input also seeds the residual stream (rows this CTA owns)
   if (kind == GV_QKV && layer == 0) {
@@ -374,14 +381,15 @@ __device__ void gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int
       p.cand_idx[cta] = best_i;
     }
   }
+  trace_mark(p, gp, cta, 2);
 }
 
 // dispatch on (KPT, RPTP) fixed at mk_create
 static __device__ void gemv_dispatch(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer, int f,
-                              int cta, int in_id, uint32_t &it, int &rb) {
+                              int cta, int in_id, uint32_t &it, int &rb, int gp) {
   const int kpt = p.geo[kind].KPT, r = p.geo[kind].RPTP;
 #define MK_GEMV_CASE(KP, RP) \
-  if (kpt == KP && r == RP) { gemv_phase<KP, RP>(p, S, ring, kind, layer, f, cta, in_id, it, rb); return; }
+  if (kpt == KP && r == RP) { gemv_phase<KP, RP>(p, S, ring, kind, layer, f, cta, in_id, it, rb, gp); return; }
 #define MK_GEMV_KPT(KP) \
   MK_GEMV_CASE(KP, 1) MK_GEMV_CASE(KP, 2) MK_GEMV_CASE(KP, 4) MK_GEMV_CASE(KP, 8) MK_GEMV_CASE(KP, 16)
   MK_GEMV_KPT(8)
@@ -456,7 +464,7 @@ __device__ __forceinline__ void norm_rope_head(const Params &p, float (&v)[HD / 
 
 template <int HD, int GRP>
 __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring, int l, int f, int cta,
-                                uint32_t &it) {
+                                uint32_t &it, int gp) {
   constexpr int EPL = HD / 32;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const AttnSched as = attn_sched(p, f);
@@ -508,6 +516,7 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
       }
     }
     cons_sync();
+    trace_mark(p, gp, cta, 1);
 
     // ---- scores and online softmax, one warp per position --------------------
     float q[GRP][EPL], o[GRP][EPL], m[GRP], ls[GRP];
@@ -618,16 +627,17 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
       }
     }
   }
+  trace_mark(p, gp, cta, 2);
 }
 
 template <int HD>
 __device__ void attention_dispatch(const Params &p, SmemCtl &S, unsigned char *ring, int l, int f, int cta,
-                                   uint32_t &it) {
+                                   uint32_t &it, int gp) {
   switch (p.grp) {
-    case 1: attention_phase<HD, 1>(p, S, ring, l, f, cta, it); break;
-    case 2: attention_phase<HD, 2>(p, S, ring, l, f, cta, it); break;
-    case 4: attention_phase<HD, 4>(p, S, ring, l, f, cta, it); break;
-    default: attention_phase<HD, 8>(p, S, ring, l, f, cta, it); break;
+    case 1: attention_phase<HD, 1>(p, S, ring, l, f, cta, it, gp); break;
+    case 2: attention_phase<HD, 2>(p, S, ring, l, f, cta, it, gp); break;
+    case 4: attention_phase<HD, 4>(p, S, ring, l, f, cta, it, gp); break;
+    default: attention_phase<HD, 8>(p, S, ring, l, f, cta, it, gp); break;
   }
 }
 
@@ -843,8 +853,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
   bool ok = true;
   for (int gp = gp_begin; gp < gp_end && ok; ++gp) {
     const int f = gp / NPH, ph = gp % NPH;
+    trace_mark(p, gp, cta, 0);
     if (ph == 5 * p.L) {
-      gemv_dispatch(p, S, ring, GV_LM, 0, f, cta, in_id, it, rb);
+      gemv_dispatch(p, S, ring, GV_LM, 0, f, cta, in_id, it, rb, gp);
     } else {
       const int l = ph / 5, k = ph % 5;
       if (k == 0 && l == 0) {
@@ -865,17 +876,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
         in_id = id;
       }
       switch (k) {
-        case 0: gemv_dispatch(p, S, ring, GV_QKV, l, f, cta, in_id, it, rb); break;
-        case 1: attention_dispatch<HD>(p, S, ring, l, f, cta, it); break;
-        case 2: gemv_dispatch(p, S, ring, GV_O, l, f, cta, in_id, it, rb); break;
-        case 3: gemv_dispatch(p, S, ring, GV_GU, l, f, cta, in_id, it, rb); break;
-        default: gemv_dispatch(p, S, ring, GV_DOWN, l, f, cta, in_id, it, rb); break;
+        case 0: gemv_dispatch(p, S, ring, GV_QKV, l, f, cta, in_id, it, rb, gp); break;
+        case 1: attention_dispatch<HD>(p, S, ring, l, f, cta, it, gp); break;
+        case 2: gemv_dispatch(p, S, ring, GV_O, l, f, cta, in_id, it, rb, gp); break;
+        case 3: gemv_dispatch(p, S, ring, GV_GU, l, f, cta, in_id, it, rb, gp); break;
+        default: gemv_dispatch(p, S, ring, GV_DOWN, l, f, cta, in_id, it, rb, gp); break;
       }
     }
     if (!p.per_op) {
       ok = grid_barrier(p, S, bar_target, bar_index++, cta);
+      trace_mark(p, gp, cta, 3);
       if (tid == 0) {
-        if (p.trace) p.trace[static_cast<size_t>(gp) * p.G + cta] = globaltimer();
         if (ph < 5 * p.L && ph % 5 == 1) st_release_cta(&S.flags[F_ATTN_DONE], f * p.L + ph / 5 + 1);
       }
     } else {
