@@ -181,6 +181,24 @@ int mk_embed_sum(const void *books, int32_t n_books, int32_t book_rows, const vo
                  int32_t text_rows, int32_t hidden, const int32_t *codes,
                  const int32_t *text_ids, int32_t n, float *out, mk_stream stream);
 
+/* mk_embed_sum for callers that cannot allocate device memory -- for example a
+ * host that runs inside another allocator's fixed memory pool, or a streaming
+ * thread that must not call cudaMalloc because it can block and synchronise the
+ * device mid-stream.  The pages have no counterpart of this entry point.
+ * Same arguments, result and errors as mk_embed_sum, and it allocates nothing:
+ * its scratch (one status word per output row) is a 16 KB static device array
+ * that every GPU loading the library holds until the process exits.
+ *   - n may be at most 4096; larger n gives MK_ERR_INVALID_ARG.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address; make that first call before any stream capture.
+ *   - All calls share the array, which keeps the last call's contents; each
+ *     call clears the words it uses.  Calls from several host threads are
+ *     serialised; calls that overlap on the GPU (e.g. issued on different
+ *     streams by other means) would race on the array. */
+int mk_embed_sum_noalloc(const void *books, int32_t n_books, int32_t book_rows, const void *text,
+                         int32_t text_rows, int32_t hidden, const int32_t *codes,
+                         const int32_t *text_ids, int32_t n, float *out, mk_stream stream);
+
 /* Free everything the handle owns (not the borrowed weights).  NULL is a no-op. */
 int mk_destroy(mk_handle *h);
 

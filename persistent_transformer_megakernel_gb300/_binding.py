@@ -64,7 +64,7 @@ class mk_info(C.Structure):
 
 #: every symbol include/mk.h declares
 EXPORTS = ("mk_create", "mk_reset_kv", "mk_decode", "mk_decode_host", "mk_get_info",
-           "mk_embed_sum", "mk_destroy", "mk_error_string")
+           "mk_embed_sum", "mk_embed_sum_noalloc", "mk_destroy", "mk_error_string")
 
 _lib = None
 
@@ -89,6 +89,7 @@ def load_library(path: Optional[str] = None):
     lib.mk_decode_host.argtypes = [vp, vp, i32, i32, vp, C.POINTER(mk_decode_opts), vp]
     lib.mk_get_info.argtypes = [vp, C.POINTER(mk_info)]
     lib.mk_embed_sum.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, i32, vp, vp]
+    lib.mk_embed_sum_noalloc.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, i32, vp, vp]
     lib.mk_destroy.argtypes = [vp]
     lib.mk_error_string.argtypes = [C.c_int]
     lib.mk_error_string.restype = C.c_char_p
