@@ -124,8 +124,9 @@ typedef struct {
                                  done, grid barrier passed; or NULL */
   int32_t attn_chunks;        /* split-KV chunks per kv head; 0 = grid / n_kv_heads */
   int64_t spin_ns;            /* budget of every device wait; 0 = 1 s */
-  int32_t fault_skip_barrier; /* test hook: CTA 0 skips its arrival at this grid barrier
-                                 (0-based, persistent path only); -1 = off */
+  int32_t fault_skip_barrier; /* test hook: CTA 0 skips its arrival at the grid barrier
+                                 that closes forward N (0-based, persistent path only);
+                                 -1 = off */
 } mk_decode_opts;
 
 typedef struct {

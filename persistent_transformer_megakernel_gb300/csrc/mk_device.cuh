@@ -147,6 +147,100 @@ __device__ __forceinline__ void trace_mark(const Params &p, int gp, int cta, int
 }
 
 // ---------------------------------------------------------------------------
+// tagged words: {float value (low 32 bits), tag (high 32 bits)} stored and
+// loaded as single 64-bit accesses, so a reader that sees the tag it expects
+// also sees the value written with it
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ll_store(unsigned long long *p, float v, unsigned tag) {
+  const unsigned long long w = (static_cast<unsigned long long>(tag) << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ unsigned long long ll_load(const unsigned long long *p) {
+  unsigned long long w;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+  return w;
+}
+__device__ __forceinline__ void ll_load2(const unsigned long long *p, unsigned long long &a,
+                                         unsigned long long &b) {
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+__device__ __forceinline__ unsigned ll_tag(unsigned long long w) { return static_cast<unsigned>(w >> 32); }
+__device__ __forceinline__ float ll_val(unsigned long long w) { return __uint_as_float(static_cast<unsigned>(w)); }
+
+// Reload the stale words of w[] (word j at src + j * STRIDE) until all carry
+// `tag`.  Gives up (values undefined) once the CTA is aborting, any CTA has
+// reported an error, or the wait budget runs out.
+template <int N, int STRIDE>
+__device__ __forceinline__ void ll_settle(const Params &p, SmemCtl &S, const unsigned long long *src,
+                                          unsigned tag, unsigned long long (&w)[N]) {
+  bool ok = true;
+#pragma unroll
+  for (int j = 0; j < N; ++j) ok &= (ll_tag(w[j]) == tag);
+  if (ok) return;
+  Deadline dl;
+  int n = 0;
+  for (;;) {
+#pragma unroll
+    for (int j = 0; j < N; ++j)
+      if (ll_tag(w[j]) != tag) w[j] = ll_load(src + j * STRIDE);
+    ok = true;
+#pragma unroll
+    for (int j = 0; j < N; ++j) ok &= (ll_tag(w[j]) == tag);
+    if (ok) return;
+    if ((++n & 15) == 0) {
+      if (flag(S, F_ABORT) || ld_relaxed_i32(p.err) != 0) return;
+      if (dl.expired(p.spin_ns)) {
+        set_err(p, MK_ERR_TIMEOUT_D);
+        flag(S, F_ABORT) = 1;
+        return;
+      }
+    }
+  }
+}
+
+// KPT consecutive tagged words -> floats (KPT even, src 16-byte aligned).  All
+// loads are issued at once; only words that still carry an older tag are
+// reloaded, tracked by a bit mask.
+template <int KPT>
+__device__ __forceinline__ void ll_poll_slice(const Params &p, SmemCtl &S, const unsigned long long *src,
+                                              unsigned tag, float (&xr)[KPT]) {
+  unsigned stale = 0;
+#pragma unroll
+  for (int c = 0; c < KPT / 2; ++c) {
+    unsigned long long a, b;
+    ll_load2(src + 2 * c, a, b);
+    xr[2 * c] = ll_val(a);
+    xr[2 * c + 1] = ll_val(b);
+    stale |= (ll_tag(a) != tag ? 1u : 0u) << (2 * c);
+    stale |= (ll_tag(b) != tag ? 1u : 0u) << (2 * c + 1);
+  }
+  if (stale == 0) return;
+  Deadline dl;
+  int n = 0;
+  for (;;) {
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      if (stale & (1u << j)) {
+        const unsigned long long wj = ll_load(src + j);
+        if (ll_tag(wj) == tag) {
+          xr[j] = ll_val(wj);
+          stale &= ~(1u << j);
+        }
+      }
+    }
+    if (stale == 0) return;
+    if ((++n & 15) == 0) {
+      if (flag(S, F_ABORT) || ld_relaxed_i32(p.err) != 0) return;
+      if (dl.expired(p.spin_ns)) {
+        set_err(p, MK_ERR_TIMEOUT_D);
+        flag(S, F_ABORT) = 1;
+        return;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // argmax helpers (largest value, lowest index among equals)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
@@ -258,23 +352,41 @@ __device__ __forceinline__ float input_elem(const Params &p, int id, int k) {
 
 // One GEMV phase of this CTA: y[r] = W[r,:] . in for the CTA's rows, with the
 // RMSNorm of the input fused in (QKV, gate/up, LM head) and the phase's
-// epilogue (store, residual add, SiLU*mul, logits + argmax candidate).
+// epilogue (publish, residual add, SiLU*mul, logits + argmax candidate).
+// Tiles are consumed without a CTA-wide barrier; row partials collect in a
+// batch buffer and one barrier per batch precedes the epilogue.
 template <int KPT, int RPTP>
 __device__ void gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer, int f,
-                           int cta, int in_id, uint32_t &it, int &rb, int gp) {
+                           int cta, int in_id, unsigned tag, uint32_t &it, int &rb, int gp) {
   const GemvGeom g = p.geo[kind];
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int kc = t % g.TPR, rg = t / g.TPR;
   const int k0 = kc * KPT;
+  const bool norm = (kind == GV_QKV || kind == GV_GU || kind == GV_LM);
+  const int qkv_rows = (p.Hq + 2 * p.Hkv) * p.d;
 
+  // ---- gains (independent of the input: their latency overlaps the poll) ---
+  float gn[KPT];
+  if (norm) {
+    const uint16_t *gain = kind == GV_QKV ? S.layers[layer].attn_norm
+                         : kind == GV_GU  ? S.layers[layer].mlp_norm
+                                          : p.final_norm;
+    load_bf16<KPT>(gain + k0, gn);
+  }
   // ---- input slice into registers ------------------------------------------
   float xr[KPT];
-  if (kind == GV_QKV && layer == 0) load_input_slice<KPT>(p, in_id, k0, xr);
-  else if (kind == GV_O) load_f32<KPT>(p.attn + k0, xr);
-  else if (kind == GV_DOWN) load_f32<KPT>(p.u + k0, xr);
-  else load_f32<KPT>(p.x + k0, xr);
-
-  if (kind == GV_QKV || kind == GV_GU || kind == GV_LM) {
+  if (kind == GV_QKV && layer == 0) {
+    load_input_slice<KPT>(p, in_id, k0, xr);
+  } else {
+    const unsigned long long *src =
+        kind == GV_QKV ? p.ll.xout + static_cast<size_t>(layer - 1) * p.H
+      : kind == GV_O   ? p.ll.attn + static_cast<size_t>(layer) * p.Hq * p.d
+      : kind == GV_GU  ? p.ll.xmid + static_cast<size_t>(layer) * p.H
+      : kind == GV_DOWN ? p.ll.u + static_cast<size_t>(layer) * p.I
+                        : p.ll.xout + static_cast<size_t>(p.L - 1) * p.H;
+    ll_poll_slice<KPT>(p, S, src + k0, tag, xr);
+  }
+  if (norm) {
     // RMSNorm fused into the GEMV: every CTA reduces mean(x^2) itself
     float ss = 0.f;
     if (rg == 0) {
@@ -288,77 +400,89 @@ __device__ void gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int
 #pragma unroll
     for (int i = 0; i < NCW; ++i) tot += S.misc[i];
     const float rs = 1.0f / sqrtf(tot / static_cast<float>(g.K) + p.eps);
-    const uint16_t *gain = kind == GV_QKV ? p.layers[layer].attn_norm
-                         : kind == GV_GU  ? p.layers[layer].mlp_norm
-                                          : p.final_norm;
 #pragma unroll
-    for (int j = 0; j < KPT; ++j) xr[j] = xr[j] * rs * bf2f(gain[k0 + j]);
-  }
-  trace_mark(p, gp, cta, 1);
-
-  // the first layer's input also seeds the residual stream (rows this CTA owns)
-  if (kind == GV_QKV && layer == 0) {
-    int o0, o1;
-    split_range(p.H, p.G, cta, o0, o1);
-    for (int r = o0 + t; r < o1; r += NCT) {
-      float v = input_elem(p, in_id, r);
-      p.x[r] = v;
-      if (p.hidden) p.hidden[(static_cast<size_t>(f) * (p.L + 1)) * p.H + r] = v;
-    }
+    for (int j = 0; j < KPT; ++j) xr[j] = xr[j] * rs * gn[j];
   }
 
   int r0, r1;
   split_range(g.rows, p.G, cta, r0, r1);
+  // the first layer's input also seeds the residual rows this CTA owns
+  if (kind == GV_QKV && layer == 0) {
+    int o0, o1;
+    split_range(p.H, p.G, cta, o0, o1);
+    for (int r = o0 + t; r < o1; r += NCT) {
+      const float v = input_elem(p, in_id, r);
+      S.xown[r - o0] = v;
+      if (p.hidden) p.hidden[(static_cast<size_t>(f) * (p.L + 1)) * p.H + r] = v;
+    }
+  }
+  trace_mark(p, gp, cta, 1);
+
   const int ntiles = (r1 - r0 + g.RT - 1) / g.RT;
   constexpr int LOGR = (RPTP >= 16) ? 4 : (RPTP >= 8) ? 3 : (RPTP >= 4) ? 2 : (RPTP >= 2) ? 1 : 0;
   const int wpr = g.TPR / 32;
+  const int wg = w % wpr;                                   // warp within its row group
+  const int trow = (kind == GV_GU) ? 2 * g.RT : g.RT;       // rows of a full tile
+  const int bt = max(1, RED_ROWS / trow);                   // tiles per epilogue batch
   float best_v = -INFINITY;
   int best_i = INT_MAX;
 
-  for (int ti = 0; ti < ntiles; ++ti) {
-    const int a = r0 + ti * g.RT;
-    const int nr = min(g.RT, r1 - a);
-    const int rows_in_tile = (kind == GV_GU) ? 2 * nr : nr;
-    const int slot = static_cast<int>(it % static_cast<uint32_t>(p.stages));
-    const uint32_t par = (it / static_cast<uint32_t>(p.stages)) & 1u;
-    wait_full(p, S, slot, par);
-    const unsigned char *st = ring + static_cast<size_t>(slot) * p.stage_bytes;
-    float acc[RPTP];
+  for (int tb = 0; tb < ntiles; tb += bt) {
+    const int te = min(ntiles, tb + bt);
+    for (int ti = tb; ti < te; ++ti) {
+      const int a = r0 + ti * g.RT;
+      const int nr = min(g.RT, r1 - a);
+      const int rows_in_tile = (kind == GV_GU) ? 2 * nr : nr;
+      const int slot = static_cast<int>(it % static_cast<uint32_t>(p.stages));
+      const uint32_t par = (it / static_cast<uint32_t>(p.stages)) & 1u;
+      wait_full(p, S, slot, par);
+      const unsigned char *st = ring + static_cast<size_t>(slot) * p.stage_bytes;
+      float acc[RPTP];
 #pragma unroll
-    for (int i = 0; i < RPTP; ++i) {
-      const int row = rg + i * g.NG;
-      acc[i] = 0.f;
-      if (row < rows_in_tile) acc[i] = dot_row<KPT>(st + (static_cast<size_t>(row) * g.K + k0) * 2, xr);
+      for (int i = 0; i < RPTP; ++i) {
+        const int row = rg + i * g.NG;
+        acc[i] = 0.f;
+        if (row < rows_in_tile) acc[i] = dot_row<KPT>(st + (static_cast<size_t>(row) * g.K + k0) * 2, xr);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[slot]);
+      const float v = warp_multi_reduce<RPTP>(acc, lane);
+      const int row = rg + (lane >> (5 - LOGR)) * g.NG;     // this lane's row inside the tile
+      if ((lane & ((32 >> LOGR) - 1)) == 0 && row < rows_in_tile) {
+        int brow;
+        if (kind == GV_GU) brow = (ti - tb) * 2 * g.RT + (row < nr ? row : g.RT + (row - nr));
+        else brow = (ti - tb) * g.RT + row;
+        S.red[rb][brow][wg] = v;
+      }
+      ++it;
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[slot]);
-    const float v = warp_multi_reduce<RPTP>(acc, lane);
-    if ((lane & ((32 >> LOGR) - 1)) == 0) S.red[rb][w][lane >> (5 - LOGR)] = v;
     cons_sync();
-    if (t < nr) {
-      auto rowsum = [&](int row) {
-        const int gq = row % g.NG, si = row / g.NG;
-        float s = 0.f;
-        for (int ww = 0; ww < wpr; ++ww) s += S.red[rb][gq * wpr + ww][si];
-        return s;
-      };
-      const float y = rowsum(t);
-      const int grow = a + t;
+    // ---- epilogue of the batch: one thread per output row (pair) ------------
+    const int a0 = r0 + tb * g.RT;
+    const int nout = min(r1, r0 + te * g.RT) - a0;
+    for (int q = t; q < nout; q += NCT) {
+      const int grow = a0 + q;
+      float y = 0.f;
+      if (kind == GV_GU) {
+        const int base = (q / g.RT) * 2 * g.RT + (q % g.RT);
+        float up = 0.f;
+        for (int ww = 0; ww < wpr; ++ww) { y += S.red[rb][base][ww]; up += S.red[rb][base + g.RT][ww]; }
+        ll_store(p.ll.u + static_cast<size_t>(layer) * p.I + grow, y / (1.0f + expf(-y)) * up, tag);
+        continue;
+      }
+      for (int ww = 0; ww < wpr; ++ww) y += S.red[rb][q][ww];
       switch (kind) {
-        case GV_QKV: p.qkv[grow] = y; break;
+        case GV_QKV: ll_store(p.ll.qkv + static_cast<size_t>(layer) * qkv_rows + grow, y, tag); break;
         case GV_O: {
-          const float xn = __ldcg(p.x + grow) + y;
-          p.x[grow] = xn;
-          break;
-        }
-        case GV_GU: {
-          const float up = rowsum(nr + t);
-          p.u[grow] = y / (1.0f + expf(-y)) * up;     // SiLU(gate) * up
+          const float xn = S.xown[grow - r0] + y;
+          S.xown[grow - r0] = xn;
+          ll_store(p.ll.xmid + static_cast<size_t>(layer) * p.H + grow, xn, tag);
           break;
         }
         case GV_DOWN: {
-          const float xn = __ldcg(p.x + grow) + y;
-          p.x[grow] = xn;
+          const float xn = S.xown[grow - r0] + y;
+          S.xown[grow - r0] = xn;
+          ll_store(p.ll.xout + static_cast<size_t>(layer) * p.H + grow, xn, tag);
           if (p.hidden) p.hidden[(static_cast<size_t>(f) * (p.L + 1) + layer + 1) * p.H + grow] = xn;
           break;
         }
@@ -371,7 +495,6 @@ __device__ void gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int
       }
     }
     rb ^= 1;
-    ++it;
   }
 
   if (kind == GV_LM) {
@@ -386,17 +509,15 @@ __device__ void gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int
 
 // dispatch on (KPT, RPTP) fixed at mk_create
 static __device__ void gemv_dispatch(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer, int f,
-                              int cta, int in_id, uint32_t &it, int &rb, int gp) {
+                              int cta, int in_id, unsigned tag, uint32_t &it, int &rb, int gp) {
   const int kpt = p.geo[kind].KPT, r = p.geo[kind].RPTP;
 #define MK_GEMV_CASE(KP, RP) \
-  if (kpt == KP && r == RP) { gemv_phase<KP, RP>(p, S, ring, kind, layer, f, cta, in_id, it, rb, gp); return; }
-#define MK_GEMV_KPT(KP) \
-  MK_GEMV_CASE(KP, 1) MK_GEMV_CASE(KP, 2) MK_GEMV_CASE(KP, 4) MK_GEMV_CASE(KP, 8) MK_GEMV_CASE(KP, 16)
-  MK_GEMV_KPT(8)
-  MK_GEMV_KPT(12)
-  MK_GEMV_KPT(16)
-  MK_GEMV_KPT(24)
-#undef MK_GEMV_KPT
+  if (kpt == KP && r == RP) { gemv_phase<KP, RP>(p, S, ring, kind, layer, f, cta, in_id, tag, it, rb, gp); return; }
+  // every (KPT, RPTP) with KPT * RPTP <= 128 (mk_create rejects the others)
+  MK_GEMV_CASE(8, 1) MK_GEMV_CASE(8, 2) MK_GEMV_CASE(8, 4) MK_GEMV_CASE(8, 8) MK_GEMV_CASE(8, 16)
+  MK_GEMV_CASE(12, 1) MK_GEMV_CASE(12, 2) MK_GEMV_CASE(12, 4) MK_GEMV_CASE(12, 8)
+  MK_GEMV_CASE(16, 1) MK_GEMV_CASE(16, 2) MK_GEMV_CASE(16, 4) MK_GEMV_CASE(16, 8)
+  MK_GEMV_CASE(24, 1) MK_GEMV_CASE(24, 2) MK_GEMV_CASE(24, 4)
 #undef MK_GEMV_CASE
 }
 
@@ -464,13 +585,15 @@ __device__ __forceinline__ void norm_rope_head(const Params &p, float (&v)[HD / 
 
 template <int HD, int GRP>
 __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring, int l, int f, int cta,
-                                uint32_t &it, int gp) {
+                                unsigned tag, uint32_t &it, int gp) {
   constexpr int EPL = HD / 32;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const AttnSched as = attn_sched(p, f);
   const int P = as.P;
   const int TP = p.stage_bytes / (4 * HD);     // positions per ring tile (K rows + V rows)
-  const LayerPtrs &LW = p.layers[l];
+  const LayerPtrs &LW = S.layers[l];
+  const unsigned long long *qkv_ll = p.ll.qkv + static_cast<size_t>(l) * (p.Hq + 2 * p.Hkv) * HD;
+  unsigned long long *attn_ll = p.ll.attn + static_cast<size_t>(l) * p.Hq * HD;
 
   for (int u = cta; u < as.units; u += p.G) {
     const int g = u / as.C, c = u % as.C;
@@ -482,18 +605,22 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
     // ---- QK-norm + RoPE of the group's queries; append K/V of position P ----
     const int njobs = GRP + (has_cur ? 2 : 0);
     for (int job = w; job < njobs; job += NCW) {
-      float v[EPL];
-      if (job < GRP) {
-        const int j = g * GRP + job;
+      // job < GRP: query head g*GRP + job; GRP: this position's key; GRP+1: its value
+      const unsigned long long *src = job < GRP ? qkv_ll + (g * GRP + job) * HD
+                                    : job == GRP ? qkv_ll + (p.Hq + g) * HD
+                                                 : qkv_ll + (p.Hq + p.Hkv + g) * HD;
+      unsigned long long wv[EPL];
 #pragma unroll
-        for (int k = 0; k < EPL; ++k) v[k] = __ldcg(p.qkv + j * HD + lane + 32 * k);
+      for (int k = 0; k < EPL; ++k) wv[k] = ll_load(src + lane + 32 * k);
+      ll_settle<EPL, 32>(p, S, src + lane, tag, wv);
+      float v[EPL];
+#pragma unroll
+      for (int k = 0; k < EPL; ++k) v[k] = ll_val(wv[k]);
+      if (job < GRP) {
         norm_rope_head<HD>(p, v, LW.q_norm, f, P, true);
 #pragma unroll
         for (int k = 0; k < EPL; ++k) S.qs[job * HD + lane + 32 * k] = v[k] * p.inv_sqrt_d;
       } else if (job == GRP) {
-        const float *src = p.qkv + p.Hq * HD + g * HD;
-#pragma unroll
-        for (int k = 0; k < EPL; ++k) v[k] = __ldcg(src + lane + 32 * k);
         norm_rope_head<HD>(p, v, LW.k_norm, f, P, true);
         uint16_t *dst = p.kcache + ((static_cast<size_t>(l) * p.Hkv + g) * p.max_seq + P) * HD;
 #pragma unroll
@@ -504,11 +631,10 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
         }
         fence_proxy_async_global();
       } else {
-        const float *src = p.qkv + (p.Hq + p.Hkv) * HD + g * HD;
         uint16_t *dst = p.vcache + ((static_cast<size_t>(l) * p.Hkv + g) * p.max_seq + P) * HD;
 #pragma unroll
         for (int k = 0; k < EPL; ++k) {
-          const uint16_t bb = f2bf(__ldcg(src + lane + 32 * k));
+          const uint16_t bb = f2bf(v[k]);
           dst[lane + 32 * k] = bb;
           S.vcur[lane + 32 * k] = bf2f(bb);
         }
@@ -588,7 +714,7 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
       }
       const int j = g * GRP + h;
       if (as.C == 1) {
-        p.attn[j * HD + i] = os / lsum;
+        ll_store(attn_ll + j * HD + i, os / lsum, tag);
       } else {
         float *dst = p.part + (static_cast<size_t>(j) * p.max_chunks + c) * (HD + 2);
         dst[i] = os;
@@ -622,7 +748,7 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
             os = fmaf(sc, __ldcg(src + cc * (HD + 2) + i), os);
             lsum = fmaf(sc, __ldcg(src + cc * (HD + 2) + HD + 1), lsum);
           }
-          p.attn[j * HD + i] = os / lsum;
+          ll_store(attn_ll + j * HD + i, os / lsum, tag);
         }
       }
     }
@@ -632,12 +758,12 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
 
 template <int HD>
 __device__ void attention_dispatch(const Params &p, SmemCtl &S, unsigned char *ring, int l, int f, int cta,
-                                   uint32_t &it, int gp) {
+                                   unsigned tag, uint32_t &it, int gp) {
   switch (p.grp) {
-    case 1: attention_phase<HD, 1>(p, S, ring, l, f, cta, it, gp); break;
-    case 2: attention_phase<HD, 2>(p, S, ring, l, f, cta, it, gp); break;
-    case 4: attention_phase<HD, 4>(p, S, ring, l, f, cta, it, gp); break;
-    default: attention_phase<HD, 8>(p, S, ring, l, f, cta, it, gp); break;
+    case 1: attention_phase<HD, 1>(p, S, ring, l, f, cta, tag, it, gp); break;
+    case 2: attention_phase<HD, 2>(p, S, ring, l, f, cta, tag, it, gp); break;
+    case 4: attention_phase<HD, 4>(p, S, ring, l, f, cta, tag, it, gp); break;
+    default: if constexpr (HD * 8 <= MAX_GRP_HD) attention_phase<HD, 8>(p, S, ring, l, f, cta, tag, it, gp); break;
   }
 }
 
@@ -694,7 +820,7 @@ struct Producer {
       if (kind == GV_QKV) {
         const int qr = p.Hq * p.d, kr = p.Hkv * p.d;
         const int segs[4] = {0, qr, qr + kr, qr + 2 * kr};
-        const uint16_t *mats[3] = {p.layers[layer].wq, p.layers[layer].wk, p.layers[layer].wv};
+        const uint16_t *mats[3] = {S.layers[layer].wq, S.layers[layer].wk, S.layers[layer].wv};
         for (int s = 0; s < 3; ++s) {
           const int lo = max(a, segs[s]), hi = min(a + nr, segs[s + 1]);
           if (lo < hi) {
@@ -704,13 +830,13 @@ struct Producer {
           }
         }
       } else if (kind == GV_GU) {
-        src[0] = p.layers[layer].w_gate + static_cast<size_t>(a) * g.K;
-        src[1] = p.layers[layer].w_up + static_cast<size_t>(a) * g.K;
+        src[0] = S.layers[layer].w_gate + static_cast<size_t>(a) * g.K;
+        src[1] = S.layers[layer].w_up + static_cast<size_t>(a) * g.K;
         bytes[0] = bytes[1] = static_cast<uint32_t>(nr) * rowb;
         n = 2;
       } else {
-        const uint16_t *base = kind == GV_O ? p.layers[layer].wo
-                             : kind == GV_DOWN ? p.layers[layer].w_down
+        const uint16_t *base = kind == GV_O ? S.layers[layer].wo
+                             : kind == GV_DOWN ? S.layers[layer].w_down
                                                : p.lm_head;
         src[0] = base + static_cast<size_t>(a) * g.K;
         bytes[0] = static_cast<uint32_t>(nr) * rowb;
@@ -739,13 +865,13 @@ struct Producer {
       const int pend = min(b, as.P);
       for (int p0 = a; p0 < pend && !stop; p0 += TP) {
         if (!guarded) {
-          // position P-1 was appended by this launch's previous forward: wait
-          // until this CTA's consumers have passed that attention phase
-          const int need = (f - 1) * p.L + l + 1;
+          // positions up to P-1 were appended by earlier forwards of this
+          // launch: wait until this CTA's consumers have passed the grid
+          // barrier that closed forward f-1
           if (f > 0) {
             Deadline dl;
             int n = 0;
-            while (ld_acquire_cta(&S.flags[F_ATTN_DONE]) < need) {
+            while (ld_acquire_cta(&S.flags[F_FWD_DONE]) < f) {
               if ((++n & 63) == 0) {
                 if (flag(S, F_ABORT)) { stop = true; return; }
                 if (dl.expired(p.spin_ns)) { set_err(p, MK_ERR_TIMEOUT_D); stop = true; return; }
@@ -805,8 +931,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
     fence_mbar_init();
     flag(S, F_ABORT) = (p.per_op && ld_relaxed_i32(p.err) != 0) ? 1 : 0;
     flag(S, F_PROD_DONE) = 0;
-    flag(S, F_ATTN_DONE) = p.per_op ? INT_MAX : 0;
+    flag(S, F_FWD_DONE) = p.per_op ? INT_MAX : 0;
     flag(S, F_LAST) = 0;
+  }
+  {
+    // the per-layer weight pointers, read by every phase, live in shared memory
+    const unsigned long long *src = reinterpret_cast<const unsigned long long *>(p.layers);
+    unsigned long long *dst = reinterpret_cast<unsigned long long *>(S.layers);
+    const int n = p.L * static_cast<int>(sizeof(LayerPtrs) / sizeof(unsigned long long));
+    for (int i = tid; i < n; i += NTHREADS) dst[i] = __ldg(src + i);
   }
   __syncthreads();
   if (flag(S, F_ABORT)) return;   // per-op launch after an earlier failure: nothing runs
@@ -845,17 +978,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
   }
 
   // -------------------------- consumer warps ----------------------------------
+  // Phases hand their outputs to the next phase as tagged words (no barrier);
+  // only the LM head ends with a grid barrier, which publishes the argmax
+  // candidates and orders this forward's KV-cache writes before the next one.
   uint32_t it = 0;
   int rb = 0;
   unsigned bar_target = 0;
-  int bar_index = 0;
   int in_id = 0;
   bool ok = true;
   for (int gp = gp_begin; gp < gp_end && ok; ++gp) {
     const int f = gp / NPH, ph = gp % NPH;
+    const unsigned tag = p.tag0 + static_cast<unsigned>(f);
     trace_mark(p, gp, cta, 0);
     if (ph == 5 * p.L) {
-      gemv_dispatch(p, S, ring, GV_LM, 0, f, cta, in_id, it, rb, gp);
+      gemv_dispatch(p, S, ring, GV_LM, 0, f, cta, in_id, tag, it, rb, gp);
+      if (!p.per_op) {
+        ok = grid_barrier(p, S, bar_target, f, cta);
+        if (tid == 0) st_release_cta(&S.flags[F_FWD_DONE], f + 1);
+      }
     } else {
       const int l = ph / 5, k = ph % 5;
       if (k == 0 && l == 0) {
@@ -876,24 +1016,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
         in_id = id;
       }
       switch (k) {
-        case 0: gemv_dispatch(p, S, ring, GV_QKV, l, f, cta, in_id, it, rb, gp); break;
-        case 1: attention_dispatch<HD>(p, S, ring, l, f, cta, it, gp); break;
-        case 2: gemv_dispatch(p, S, ring, GV_O, l, f, cta, in_id, it, rb, gp); break;
-        case 3: gemv_dispatch(p, S, ring, GV_GU, l, f, cta, in_id, it, rb, gp); break;
-        default: gemv_dispatch(p, S, ring, GV_DOWN, l, f, cta, in_id, it, rb, gp); break;
+        case 0: gemv_dispatch(p, S, ring, GV_QKV, l, f, cta, in_id, tag, it, rb, gp); break;
+        case 1: attention_dispatch<HD>(p, S, ring, l, f, cta, tag, it, gp); break;
+        case 2: gemv_dispatch(p, S, ring, GV_O, l, f, cta, in_id, tag, it, rb, gp); break;
+        case 3: gemv_dispatch(p, S, ring, GV_GU, l, f, cta, in_id, tag, it, rb, gp); break;
+        default: gemv_dispatch(p, S, ring, GV_DOWN, l, f, cta, in_id, tag, it, rb, gp); break;
       }
     }
-    if (!p.per_op) {
-      ok = grid_barrier(p, S, bar_target, bar_index++, cta);
-      trace_mark(p, gp, cta, 3);
-      if (tid == 0) {
-        if (ph < 5 * p.L && ph % 5 == 1) st_release_cta(&S.flags[F_ATTN_DONE], f * p.L + ph / 5 + 1);
-      }
-    } else {
+    trace_mark(p, gp, cta, 3);
+    if (p.per_op) {
       cons_sync();
       ok = flag(S, F_ABORT) == 0;
     }
   }
+  cons_sync();
   if (ok && final_select && flag(S, F_ABORT) == 0) select_token(p, S, p.n_fwd - 1, cta, true);
 
   // ---- shutdown: stop the producer and wait until its copies have landed ----

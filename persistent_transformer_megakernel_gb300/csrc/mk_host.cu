@@ -24,7 +24,7 @@
 namespace {
 
 constexpr int kStageBytes = 32 * 1024;
-constexpr int kStages = 6;
+constexpr int kMaxStagesWanted = 6;
 constexpr int kMinChunks = 64;   // split-KV chunk capacity per kv head (at least grid / Hkv)
 
 struct DeviceBuffers {
@@ -84,7 +84,7 @@ int make_geom(int K, int rows, bool pairs, mk::GemvGeom &g) {
     if (g.RT < 1) return MK_ERR_UNSUPPORTED;
     g.RPTP = pow2_at_least((g.RT + g.NG - 1) / g.NG);
   }
-  if (g.RPTP > 16) return MK_ERR_UNSUPPORTED;
+  if (g.RPTP > 16 || g.KPT * g.RPTP > 128) return MK_ERR_UNSUPPORTED;
   g.rows = rows;
   return MK_OK;
 }
@@ -100,6 +100,10 @@ struct mk_handle {
   int smem = 0;
   int pos = 0;
   int max_chunks = 0;
+  int stages = 0;
+  unsigned tag = 1;          // tag of the next forward's published activations
+  size_t ll_words = 0;
+  unsigned long long *ll_base = nullptr;
   int64_t weight_bytes = 0, kv_bytes = 0;
   const void *kernel = nullptr;
   DeviceBuffers buf;
@@ -139,6 +143,7 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
   const int grp = c.n_q_heads / c.n_kv_heads;
   if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return MK_ERR_UNSUPPORTED;
   if (grp * c.head_dim > mk::MAX_GRP_HD) return MK_ERR_UNSUPPORTED;
+  if (c.n_layers > mk::MAX_LAYERS) return MK_ERR_UNSUPPORTED;
   if (c.rope_mode != 0 && c.rope_mode != 1) return MK_ERR_INVALID_ARG;
   if (c.rope_mode == 1) {
     if (c.mrope_sections[0] < 0 || c.mrope_sections[1] < 0 || c.mrope_sections[2] < 0 ||
@@ -182,8 +187,16 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
   if (!coop) return fail(MK_ERR_UNSUPPORTED);
   h->G = prop.multiProcessorCount;
   h->kernel = (d == 64) ? mk::kernel_d64() : mk::kernel_d128();
-  h->smem = mk::RING_OFFSET + kStages * kStageBytes;
-  if (h->smem > static_cast<int>(prop.sharedMemPerBlockOptin)) return fail(MK_ERR_UNSUPPORTED);
+  // residual rows owned per CTA, and rows of every phase, must fit the static buffers
+  if ((H + h->G - 1) / h->G > mk::MAX_OWN) return fail(MK_ERR_UNSUPPORTED);
+  for (int k = 0; k < mk::GV_COUNT; ++k) {
+    const int trow = (k == mk::GV_GU) ? 2 * geo[k].RT : geo[k].RT;
+    if (trow > mk::RED_ROWS || geo[k].TPR / 32 > mk::MAX_WPR) return fail(MK_ERR_UNSUPPORTED);
+  }
+  h->stages = std::min(kMaxStagesWanted,
+                       (static_cast<int>(prop.sharedMemPerBlockOptin) - mk::RING_OFFSET) / kStageBytes);
+  if (h->stages < 2) return fail(MK_ERR_UNSUPPORTED);
+  h->smem = mk::RING_OFFSET + h->stages * kStageBytes;
   if (cudaFuncSetAttribute(h->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, h->smem) != cudaSuccess) {
     cudaGetLastError();
     return fail(MK_ERR_CUDA);
@@ -202,17 +215,15 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
   mk::LayerPtrs *d_layers = nullptr;
   uint16_t *kc = nullptr, *vc = nullptr;
   float2 *rope = nullptr;
-  float *x = nullptr, *qkv = nullptr, *attn = nullptr, *u = nullptr, *part = nullptr, *cand_val = nullptr;
+  float *part = nullptr, *cand_val = nullptr;
   int *cand_idx = nullptr;
   unsigned *tickets = nullptr;
   if ((rc = h->buf.alloc((void **)&d_layers, sizeof(mk::LayerPtrs) * c.n_layers)) ||
       (rc = h->buf.alloc((void **)&kc, kv_elems * 2)) ||
       (rc = h->buf.alloc((void **)&vc, kv_elems * 2)) ||
       (rc = h->buf.alloc((void **)&rope, sizeof(float2) * static_cast<size_t>(rope_len) * (d / 2))) ||
-      (rc = h->buf.alloc((void **)&x, sizeof(float) * H)) ||
-      (rc = h->buf.alloc((void **)&qkv, sizeof(float) * (Hq + 2 * Hkv) * d)) ||
-      (rc = h->buf.alloc((void **)&attn, sizeof(float) * Hq * d)) ||
-      (rc = h->buf.alloc((void **)&u, sizeof(float) * I)) ||
+      (rc = h->buf.alloc((void **)&h->ll_base, sizeof(unsigned long long) *
+                         (h->ll_words = static_cast<size_t>(c.n_layers) * ((Hq + 2 * Hkv) * d + Hq * d + 2 * H + I)))) ||
       (rc = h->buf.alloc((void **)&part, sizeof(float) * static_cast<size_t>(Hq) * h->max_chunks * (d + 2))) ||
       (rc = h->buf.alloc((void **)&cand_val, sizeof(float) * h->G)) ||
       (rc = h->buf.alloc((void **)&cand_idx, sizeof(int) * h->G)) ||
@@ -244,6 +255,7 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
       cudaMemset(tickets, 0, sizeof(unsigned) * Hkv) != cudaSuccess ||
       cudaMemset(h->d_sync, 0, sizeof(int) * 4) != cudaSuccess ||
       cudaMemset(kc, 0, kv_elems * 2) != cudaSuccess || cudaMemset(vc, 0, kv_elems * 2) != cudaSuccess ||
+      cudaMemset(h->ll_base, 0, sizeof(unsigned long long) * h->ll_words) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();
     return fail(MK_ERR_CUDA);
@@ -266,13 +278,22 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
   p.lm_head = (const uint16_t *)(w->lm_head ? w->lm_head : w->embed);
   p.final_norm = (const uint16_t *)w->final_norm;
   p.kcache = kc; p.vcache = vc; p.rope = rope;
-  p.x = x; p.qkv = qkv; p.attn = attn; p.u = u; p.part = part;
+  {
+    unsigned long long *q = h->ll_base;
+    const size_t Lc = static_cast<size_t>(c.n_layers);
+    p.ll.qkv = q;  q += Lc * (Hq + 2 * Hkv) * d;
+    p.ll.attn = q; q += Lc * Hq * d;
+    p.ll.xmid = q; q += Lc * H;
+    p.ll.u = q;    q += Lc * I;
+    p.ll.xout = q;
+  }
+  p.part = part;
   p.cand_val = cand_val; p.cand_idx = cand_idx; p.tickets = tickets;
   p.bar = reinterpret_cast<unsigned *>(h->d_sync);
   p.err = h->d_sync + 1;
   p.last_id = h->d_sync + 2;
   p.G = h->G;
-  p.stages = kStages;
+  p.stages = h->stages;
   p.stage_bytes = kStageBytes;
   for (int k = 0; k < mk::GV_COUNT; ++k) p.geo[k] = geo[k];
 
@@ -330,6 +351,16 @@ int mk_decode(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_ste
   p.fault_barrier = o.fault_skip_barrier;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // every forward publishes its activations under a tag never used before
+  if (h->tag > 0xF0000000u - static_cast<unsigned>(n_fwd)) {
+    if (cudaMemsetAsync(h->ll_base, 0, sizeof(unsigned long long) * h->ll_words, s) != cudaSuccess) {
+      cudaGetLastError();
+      return MK_ERR_CUDA;
+    }
+    h->tag = 1;
+  }
+  p.tag0 = h->tag;
+  h->tag += static_cast<unsigned>(n_fwd);
   // barrier counter, error word and merge tickets start at zero for every call
   if (cudaMemsetAsync(h->d_sync, 0, sizeof(int) * 2, s) != cudaSuccess ||
       cudaMemsetAsync(h->base.tickets, 0, sizeof(unsigned) * h->cfg.n_kv_heads, s) != cudaSuccess) {
@@ -401,7 +432,7 @@ int mk_get_info(const mk_handle *h, mk_info *info) {
   if (!h || !info) return MK_ERR_INVALID_ARG;
   info->grid = h->G;
   info->threads = mk::NTHREADS;
-  info->stages = kStages;
+  info->stages = h->stages;
   info->stage_bytes = kStageBytes;
   info->smem_bytes = h->smem;
   info->position = h->pos;

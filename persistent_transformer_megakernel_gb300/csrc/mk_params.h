@@ -1,25 +1,35 @@
-// Launch parameters shared by the host library and the device code.
+// Launch parameters and shared-memory layout shared by the host library and
+// the device code.
 #pragma once
 #include <cstdint>
 
+#ifndef MK_NCW
+#define MK_NCW 8
+#endif
+
 namespace mk {
 
-constexpr int NCW = 8;               // consumer warps per CTA
+constexpr int NCW = MK_NCW;          // consumer warps per CTA
 constexpr int NCT = NCW * 32;        // consumer threads
 constexpr int NTHREADS = NCT + 32;   // + one TMA producer warp
 constexpr int MAX_STAGES = 8;
+constexpr int MAX_LAYERS = 64;
+constexpr int MAX_OWN = 64;          // residual rows one CTA may own (H / grid, rounded up)
+constexpr int RED_ROWS = 64;         // rows of one GEMV epilogue batch
+constexpr int MAX_WPR = 8;           // warps that share one row (threads per row / 32)
+constexpr int MAX_GRP_HD = 256;      // group size * head_dim handled by one attention unit
 
 // GEMV phases in the order of their geometry table
 enum GemvKind { GV_QKV = 0, GV_O = 1, GV_GU = 2, GV_DOWN = 3, GV_LM = 4, GV_COUNT = 5 };
 
-// how a GEMV phase maps rows and the input width onto the consumer threads:
-// thread t owns KPT consecutive input elements (k-chunk t % TPR) of NG = 256/TPR
+// How a GEMV phase maps rows and the input width onto the consumer threads:
+// thread t owns KPT consecutive input elements (k-chunk t % TPR) of NG = NCT/TPR
 // row groups; a tile holds RT rows (GU: RT gate/up row pairs).
 struct GemvGeom {
   int K;        // input width
   int KPT;      // input elements per thread (8, 12, 16, 24)
   int TPR;      // threads per row (32, 64, 128, 256)
-  int NG;       // row groups = 256 / TPR
+  int NG;       // row groups = NCT / TPR
   int RT;       // rows (pairs for GU) per ring tile
   int RPTP;     // rows per thread per tile, padded to a power of two (<= 16)
   int rows;     // total rows (pairs for GU) of the phase
@@ -28,6 +38,18 @@ struct GemvGeom {
 struct LayerPtrs {
   const uint16_t *attn_norm, *wq, *wk, *wv, *q_norm, *k_norm, *wo;
   const uint16_t *mlp_norm, *w_gate, *w_up, *w_down;
+};
+
+// Activations crossing CTAs travel as 64-bit words {float value, 32-bit tag};
+// the tag names the forward that wrote them, so a reader polls a word until it
+// carries the tag it expects.  One buffer per layer and kind, reused only by
+// the next forward (after the grid barrier that closes every forward).
+struct LLBuffers {
+  unsigned long long *qkv;    // [L][(Hq + 2 Hkv) d]  raw q, k, v
+  unsigned long long *attn;   // [L][Hq d]            attention output
+  unsigned long long *xmid;   // [L][H]               residual after attention
+  unsigned long long *u;      // [L][I]               SiLU(gate) * up
+  unsigned long long *xout;   // [L][H]               residual after the MLP
 };
 
 struct Params {
@@ -42,7 +64,8 @@ struct Params {
   // handle-owned state and scratch
   uint16_t *kcache, *vcache;       // [L][Hkv][max_seq][d]
   const float2 *rope;              // [rope_len][d/2] (cos, sin)
-  float *x, *qkv, *attn, *u, *part, *cand_val;
+  LLBuffers ll;
+  float *part, *cand_val;
   int *cand_idx;
   unsigned *tickets;               // [Hkv]
   unsigned *bar;                   // grid-barrier counter (zeroed before each launch)
@@ -51,6 +74,7 @@ struct Params {
   // this call
   const int32_t *in_ids;
   int n_in, n_fwd, pos0;
+  unsigned tag0;                   // tag of forward 0 of this call (nonzero, increasing)
   int32_t *out_ids;
   const float *embeds;
   int n_embed_rows;
@@ -67,28 +91,24 @@ struct Params {
   GemvGeom geo[GV_COUNT];
 };
 
-}  // namespace mk
-
-namespace mk {
-
 // flags shared inside a CTA between the consumer warps and the producer lane
-enum SmemFlag { F_ABORT = 0, F_PROD_DONE = 1, F_ATTN_DONE = 2, F_LAST = 3, F_TOKEN = 4, F_COUNT = 8 };
-
-constexpr int MAX_GRP_HD = 512;   // group size * head_dim handled by one attention unit
+enum SmemFlag { F_ABORT = 0, F_PROD_DONE = 1, F_FWD_DONE = 2, F_LAST = 3, F_COUNT = 8 };
 
 // static part of the dynamic shared memory; the weight ring follows at RING_OFFSET
 struct SmemCtl {
   uint64_t full[MAX_STAGES];
   uint64_t empty[MAX_STAGES];
-  float red[2][NCW][32];            // per-warp row partials, double buffered by tile
+  LayerPtrs layers[MAX_LAYERS];          // pointer table copied at kernel start
+  float red[2][RED_ROWS][MAX_WPR];       // per-warp row partials of one epilogue batch
   float misc[64];
+  float xown[MAX_OWN];                   // residual rows this CTA owns
   int flags[F_COUNT];
   float bestv[NCW];
   int besti[NCW];
-  float qs[MAX_GRP_HD];             // normed, rotated, scaled queries of one unit
-  float kcur[128], vcur[128];       // this position's key / value (bf16-rounded)
-  float ow[NCW][MAX_GRP_HD];        // per-warp unnormalised attention outputs
-  float mw[NCW][8], lw[NCW][8];     // per-warp running max / sum per head
+  float qs[MAX_GRP_HD];                  // normed, rotated, scaled queries of one unit
+  float kcur[128], vcur[128];            // this position's key / value (bf16-rounded)
+  float ow[NCW][MAX_GRP_HD];             // per-warp unnormalised attention outputs
+  float mw[NCW][8], lw[NCW][8];          // per-warp running max / sum per head
 };
 
 constexpr int RING_OFFSET = (int)((sizeof(SmemCtl) + 1023) / 1024 * 1024);

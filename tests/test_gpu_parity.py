@@ -179,10 +179,10 @@ def test_errors_are_reported_not_raised_as_faults():
         dec.decode([1, 2, 3], 6)                                  # 9 forwards > max_seq 8
     assert e.value.code == -3
     dec.reset()
-    # a CTA that never arrives at a grid barrier: the others give up after the
-    # wait budget and the call returns a timeout instead of hanging
+    # a CTA that never arrives at the grid barrier closing forward 1: the
+    # others give up after the wait budget and the call returns a timeout
     with pytest.raises(mk.MKError) as e:
-        dec.decode([1, 2], 0, spin_ns=20_000_000, fault_skip_barrier=3)
+        dec.decode([1, 2], 1, spin_ns=20_000_000, fault_skip_barrier=1)
     assert e.value.code == -5
     dec.reset()
     ids = dec.decode([1, 2], 2)                                   # the handle still works
