@@ -1,0 +1,139 @@
+"""Parity at the workloads' full model sizes, in the launch configuration the
+bench uses (one CTA per SM, one cooperative launch for a whole call).
+
+The oracle generates its own greedy id stream; the CUDA path then runs
+teacher-forced on those ids (oracle -> GPU only), so that every forward's
+logits, per-layer hidden states and greedy id are comparable one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+from parity_util import assert_close, assert_ids, first_near_tie
+
+pytestmark = pytest.mark.gpu
+
+mk = pytest.importorskip("persistent_transformer_megakernel_gb300")
+
+
+def _gpu_teacher_forced(dec, feed, embeds=None, pos3=None, hidden=True):
+    s = dec.shape
+    n = len(feed)
+    logits = torch.full((n, s["vocab"]), float("nan"), dtype=torch.float32, device="cuda:0")
+    hid = None
+    if hidden:
+        hid = torch.full((n, s["n_layers"] + 1, s["hidden"]), float("nan"), dtype=torch.float32,
+                         device="cuda:0")
+    ids = dec.decode(feed, 0, logits=logits, hidden=hid, embeds=embeds, pos3=pos3)
+    torch.cuda.synchronize()
+    return (ids.cpu().numpy(), logits.double().cpu().numpy(),
+            None if hid is None else hid.double().cpu().numpy())
+
+
+def _compare(name, s, ids, lg, hd, ids_ref, lg_ref, hd_ref):
+    assert_close(lg, lg_ref, name + " logits")
+    if hd is not None:
+        for l in range(s["n_layers"] + 1):
+            assert_close(hd[:, l], hd_ref[:, l], "%s hidden[%d]" % (name, l))
+    assert_ids(ids, ids_ref, lg_ref, name + " ids")
+
+
+def test_qwen3_0p6b_prompt32_greedy512():
+    # the bench workload: 32 prompt forwards + 512 greedy forwards
+    s = W.shape("qwen3_0p6b")
+    w = W.make_weights(s, seed=0)
+    prompt = W.make_prompt(s["vocab_in"], 32, seed=1)
+    ref = O.Decoder(s, w, max_seq=544)
+    ids_ref, lg_ref, hd_ref = ref.generate(prompt, 512)
+    del ref
+    feed = np.concatenate([prompt, ids_ref[31:543]]).astype(np.int32)
+    dec = mk.Decoder(s, w, max_seq=544)
+    ids, lg, hd = _gpu_teacher_forced(dec, feed)
+    _compare("qwen3_0p6b", s, ids, lg, hd, ids_ref, lg_ref, hd_ref)
+    # free-running greedy in one launch: identical up to the oracle's first near tie
+    dec.reset()
+    free = dec.decode(prompt, 512).cpu().numpy()
+    k = first_near_tie(lg_ref)
+    assert np.array_equal(free[:k], ids_ref[:k]), "greedy ids diverge before the first near tie (%d)" % k
+    dec.close()
+
+
+def test_tts_talker_sentinel_mrope_256():
+    # talker: untied 3072-entry head, MRoPE (24, 20, 20) with three distinct
+    # position streams, every input the 17-way embedding sum via a sentinel id
+    s = W.shape("tts_talker")
+    w = W.make_weights(s, seed=0)
+    n = 256
+    tables = W.make_tts_tables(s["hidden"], seed=3)
+    codes, text = W.make_tts_codes(n, seed=2)
+    E_ref = O.embed_sum17(tables["codebooks"], tables["text"], codes, text)
+    books = torch.from_numpy(tables["codebooks"].view(np.int16)).view(torch.bfloat16).cuda()
+    txt = torch.from_numpy(tables["text"].view(np.int16)).view(torch.bfloat16).cuda()
+    E = mk.embed_sum(books, txt, torch.as_tensor(codes).cuda(), torch.as_tensor(text).cuda())
+    torch.cuda.synchronize()
+    assert_close(E.double().cpu().numpy(), E_ref, "17-way embedding sum")
+    del books, txt
+    pos3 = W.make_pos3(0, n, distinct=True)
+    sid = W.sentinel_ids(n)
+    ref = O.Decoder(s, w, max_seq=n)
+    ids_ref, lg_ref, hd_ref = ref.generate(sid, 0, sentinel_rows=E_ref, pos3=pos3)
+    dec = mk.Decoder(s, w, max_seq=n)
+    ids, lg, hd = _gpu_teacher_forced(dec, sid, embeds=E, pos3=torch.as_tensor(pos3, device="cuda:0"))
+    _compare("tts_talker", s, ids, lg, hd, ids_ref, lg_ref, hd_ref)
+    dec.close()
+
+
+def test_qwen3_1p7b_prompt32_greedy96():
+    s = W.shape("qwen3_1p7b")
+    w = W.make_weights(s, seed=0)
+    prompt = W.make_prompt(s["vocab_in"], 32, seed=1)
+    ref = O.Decoder(s, w, max_seq=128)
+    ids_ref, lg_ref, hd_ref = ref.generate(prompt, 96)
+    del ref
+    feed = np.concatenate([prompt, ids_ref[31:127]]).astype(np.int32)
+    dec = mk.Decoder(s, w, max_seq=128)
+    ids, lg, hd = _gpu_teacher_forced(dec, feed)
+    _compare("qwen3_1p7b", s, ids, lg, hd, ids_ref, lg_ref, hd_ref)
+    dec.close()
+
+
+def test_long_context_4096_prompt_then_greedy():
+    # long-context workload at its prompt length: the oracle computes the 4096
+    # prompt positions with its all-positions path, then continues step by step
+    s = W.shape("qwen3_0p6b")
+    w = W.make_weights(s, seed=0)
+    T, n_steps = 4096, 8
+    prompt = W.make_prompt(s["vocab_in"], T, seed=1)
+    shp = O.DecoderShape.from_dict(s)
+    Wt = O.decoder.Weights(shp, w)
+    pl, _, Kp, Vp = O.prefix_forward(shp, None, prompt, logits_for=[T - 1], weights=Wt)
+    ref = O.Decoder(shp, None, max_seq=T + n_steps, weights=Wt)
+    ref.K[:, :, :T] = Kp
+    ref.V[:, :, :T] = Vp
+    ref.pos = T
+    ref.last_id = O.argmax_lowest(pl[0])
+    del Kp, Vp
+    ids_ref, lg_ref, hd_ref = ref.generate([], n_steps)
+    # GPU: the prompt in one launch, then the greedy forwards teacher-forced
+    dec = mk.Decoder(s, w, max_seq=T + n_steps)
+    last_prompt_id = int(dec.decode(prompt, 0).cpu().numpy()[-1])
+    top = np.argsort(pl[0])[-2:]
+    if pl[0][top[1]] - pl[0][top[0]] > 1e-2:
+        assert last_prompt_id == ref.last_id or last_prompt_id == int(top[1])
+    else:
+        assert last_prompt_id in top
+    feed = np.concatenate([[O.argmax_lowest(pl[0])], ids_ref[:n_steps - 1]]).astype(np.int32)
+    ids, lg, hd = _gpu_teacher_forced(dec, feed)
+    _compare("long_ctx", s, ids, lg, hd, ids_ref, lg_ref, hd_ref)
+    dec.close()
+    # at this context the split-KV result does not depend on the chunk count
+    one = mk.Decoder(s, w, max_seq=T + n_steps)
+    one.decode(prompt, 0, attn_chunks=1)
+    n = len(feed)
+    lg1 = torch.full((n, s["vocab"]), float("nan"), dtype=torch.float32, device="cuda:0")
+    one.decode(feed, 0, logits=lg1, attn_chunks=1)
+    torch.cuda.synchronize()
+    lg1 = lg1.double().cpu().numpy()
+    assert np.abs(lg1 - lg).max() <= 1e-3 * max(1.0, np.abs(lg).max())
