@@ -32,6 +32,35 @@ import workloads as W  # noqa: E402
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
+CSRC = os.path.join(ROOT, "persistent_transformer_megakernel_gb300", "csrc")
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def kernel_sources_sha256():
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for path in sorted(glob.glob(os.path.join(CSRC, "*"))):
+        h.update(os.path.basename(path).encode())
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload, forwards_per_launch):
+    """DRAM bytes (read + write) per launch from the ncu record of this
+    workload, scaled by forwards; None when there is no record or the kernel
+    sources changed since it was taken."""
+    path = os.path.join(PROFILES, "traffic_%s.json" % workload)
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("kernel_sources_sha256") != kernel_sources_sha256():
+        return None
+    per_fwd = (rec["dram_bytes_read"] + rec["dram_bytes_write"]) / rec["captured_forwards"]
+    return per_fwd * forwards_per_launch
 
 
 def workload_desc(name):
@@ -343,7 +372,7 @@ def run_gpu(args, rank, world):
                    "ring": "%d x %d KB" % (info["stages"], info["stage_bytes"] // 1024),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": measured_traffic(args.workload, n_timed),
                      "peak_source": "%s hbm_gbs (copy bandwidth)" % peak_src,
                      "algorithmic_bytes_per_launch": bytes_launch,
                      "kernel": "mk::mk_decode_kernel<%d>" % s["head_dim"]},
@@ -358,6 +387,20 @@ def run_gpu(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def ncu_case(args):
+    """The small case the ncu captures use: one 16-token prompt launch, then
+    one launch of 8 greedy forwards (the captured one, ``-s 1 -c 1``)."""
+    import torch
+    import persistent_transformer_megakernel_gb300 as mk
+    wl, s, _ = workload_desc(args.workload)
+    w = W.make_weights(s, seed=0)
+    dec = mk.Decoder(s, w, max_seq=64)
+    dec.decode(W.make_prompt(s["vocab_in"], 16, seed=1), 0)
+    dec.decode(None, 8)
+    torch.cuda.synchronize()
+    print("ncu case done: %s, 16 prompt forwards then 8 greedy forwards" % args.workload)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -369,7 +412,12 @@ def main():
     ap.add_argument("--ablation-forwards", type=int, default=32)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-ablation", action="store_true")
+    ap.add_argument("--ncu-case", action="store_true",
+                    help="run only the small profiling case (no JSON line)")
     args = ap.parse_args()
+    if args.ncu_case:
+        ncu_case(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
