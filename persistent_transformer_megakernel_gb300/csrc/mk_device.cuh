@@ -155,6 +155,10 @@ __device__ __forceinline__ void ll_store(unsigned long long *p, float v, unsigne
   const unsigned long long w = (static_cast<unsigned long long>(tag) << 32) | __float_as_uint(v);
   asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
 }
+// publish to every copy of a tagged buffer
+__device__ __forceinline__ void ll_store_rep(const Params &p, unsigned long long *dst, float v, unsigned tag) {
+  for (int r = 0; r < p.ll_rep; ++r) ll_store(dst + r * p.ll_cs, v, tag);
+}
 __device__ __forceinline__ unsigned long long ll_load(const unsigned long long *p) {
   unsigned long long w;
   asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
@@ -187,6 +191,7 @@ __device__ __forceinline__ void ll_settle(const Params &p, SmemCtl &S, const uns
 #pragma unroll
     for (int j = 0; j < N; ++j) ok &= (ll_tag(w[j]) == tag);
     if (ok) return;
+    if (p.poll_ns) __nanosleep(p.poll_ns);
     if ((++n & 15) == 0) {
       if (flag(S, F_ABORT) || ld_relaxed_i32(p.err) != 0) return;
       if (dl.expired(p.spin_ns)) {
@@ -229,6 +234,7 @@ __device__ __forceinline__ void ll_poll_slice(const Params &p, SmemCtl &S, const
       }
     }
     if (stale == 0) return;
+    if (p.poll_ns) __nanosleep(p.poll_ns);
     if ((++n & 15) == 0) {
       if (flag(S, F_ABORT) || ld_relaxed_i32(p.err) != 0) return;
       if (dl.expired(p.spin_ns)) {
@@ -384,7 +390,7 @@ __device__ void gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int
       : kind == GV_GU  ? p.ll.xmid + static_cast<size_t>(layer) * p.H
       : kind == GV_DOWN ? p.ll.u + static_cast<size_t>(layer) * p.I
                         : p.ll.xout + static_cast<size_t>(p.L - 1) * p.H;
-    ll_poll_slice<KPT>(p, S, src + k0, tag, xr);
+    ll_poll_slice<KPT>(p, S, src + (cta % p.ll_rep) * p.ll_cs + k0, tag, xr);
   }
   if (norm) {
     // RMSNorm fused into the GEMV: every CTA reduces mean(x^2) itself
@@ -467,22 +473,22 @@ __device__ void gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int
         const int base = (q / g.RT) * 2 * g.RT + (q % g.RT);
         float up = 0.f;
         for (int ww = 0; ww < wpr; ++ww) { y += S.red[rb][base][ww]; up += S.red[rb][base + g.RT][ww]; }
-        ll_store(p.ll.u + static_cast<size_t>(layer) * p.I + grow, y / (1.0f + expf(-y)) * up, tag);
+        ll_store_rep(p, p.ll.u + static_cast<size_t>(layer) * p.I + grow, y / (1.0f + expf(-y)) * up, tag);
         continue;
       }
       for (int ww = 0; ww < wpr; ++ww) y += S.red[rb][q][ww];
       switch (kind) {
-        case GV_QKV: ll_store(p.ll.qkv + static_cast<size_t>(layer) * qkv_rows + grow, y, tag); break;
+        case GV_QKV: ll_store_rep(p, p.ll.qkv + static_cast<size_t>(layer) * qkv_rows + grow, y, tag); break;
         case GV_O: {
           const float xn = S.xown[grow - r0] + y;
           S.xown[grow - r0] = xn;
-          ll_store(p.ll.xmid + static_cast<size_t>(layer) * p.H + grow, xn, tag);
+          ll_store_rep(p, p.ll.xmid + static_cast<size_t>(layer) * p.H + grow, xn, tag);
           break;
         }
         case GV_DOWN: {
           const float xn = S.xown[grow - r0] + y;
           S.xown[grow - r0] = xn;
-          ll_store(p.ll.xout + static_cast<size_t>(layer) * p.H + grow, xn, tag);
+          ll_store_rep(p, p.ll.xout + static_cast<size_t>(layer) * p.H + grow, xn, tag);
           if (p.hidden) p.hidden[(static_cast<size_t>(f) * (p.L + 1) + layer + 1) * p.H + grow] = xn;
           break;
         }
@@ -518,6 +524,8 @@ static __device__ void gemv_dispatch(const Params &p, SmemCtl &S, unsigned char 
   MK_GEMV_CASE(12, 1) MK_GEMV_CASE(12, 2) MK_GEMV_CASE(12, 4) MK_GEMV_CASE(12, 8)
   MK_GEMV_CASE(16, 1) MK_GEMV_CASE(16, 2) MK_GEMV_CASE(16, 4) MK_GEMV_CASE(16, 8)
   MK_GEMV_CASE(24, 1) MK_GEMV_CASE(24, 2) MK_GEMV_CASE(24, 4)
+  if constexpr (KPT_MAX >= 32) { MK_GEMV_CASE(32, 1) MK_GEMV_CASE(32, 2) MK_GEMV_CASE(32, 4) }
+  if constexpr (KPT_MAX >= 48) { MK_GEMV_CASE(48, 1) MK_GEMV_CASE(48, 2) }
 #undef MK_GEMV_CASE
 }
 
@@ -592,7 +600,8 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
   const int P = as.P;
   const int TP = p.stage_bytes / (4 * HD);     // positions per ring tile (K rows + V rows)
   const LayerPtrs &LW = S.layers[l];
-  const unsigned long long *qkv_ll = p.ll.qkv + static_cast<size_t>(l) * (p.Hq + 2 * p.Hkv) * HD;
+  const unsigned long long *qkv_ll = p.ll.qkv + static_cast<size_t>(l) * (p.Hq + 2 * p.Hkv) * HD +
+                                     (cta % p.ll_rep) * p.ll_cs;
   unsigned long long *attn_ll = p.ll.attn + static_cast<size_t>(l) * p.Hq * HD;
 
   for (int u = cta; u < as.units; u += p.G) {
@@ -714,7 +723,7 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
       }
       const int j = g * GRP + h;
       if (as.C == 1) {
-        ll_store(attn_ll + j * HD + i, os / lsum, tag);
+        ll_store_rep(p, attn_ll + j * HD + i, os / lsum, tag);
       } else {
         float *dst = p.part + (static_cast<size_t>(j) * p.max_chunks + c) * (HD + 2);
         dst[i] = os;
@@ -748,7 +757,7 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
             os = fmaf(sc, __ldcg(src + cc * (HD + 2) + i), os);
             lsum = fmaf(sc, __ldcg(src + cc * (HD + 2) + HD + 1), lsum);
           }
-          ll_store(attn_ll + j * HD + i, os / lsum, tag);
+          ll_store_rep(p, attn_ll + j * HD + i, os / lsum, tag);
         }
       }
     }

@@ -13,6 +13,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -46,17 +47,20 @@ struct DeviceBuffers {
   }
 };
 
+// input elements per thread and threads per row of a GEMV with input width K:
+// K = KPT * TPR with TPR a whole number of warps dividing the consumer threads;
+// the largest KPT up to MK_KPT_MAX (fewer, longer per-thread dot products)
 int choose_kpt(int K, int &kpt, int &tpr) {
-  static const int kpts[] = {8, 12, 16, 24};
-  for (int c : kpts) {
-    if (K % c) continue;
+  static const int kpts[] = {48, 32, 24, 16, 12, 8};
+  auto ok = [&](int c) {
+    if (K % c) return false;
     const int t = K / c;
-    if (t == 32 || t == 64 || t == 128 || t == 256) {
-      kpt = c;
-      tpr = t;
-      return MK_OK;
-    }
-  }
+    return t >= 32 && t <= mk::NCT && t % 32 == 0 && mk::NCT % t == 0;
+  };
+  for (int c : kpts)                       // widest slice allowed
+    if (c <= mk::KPT_MAX && ok(c)) { kpt = c; tpr = K / c; return MK_OK; }
+  for (int i = 5; i >= 0; --i)             // otherwise the narrowest that fits
+    if (ok(kpts[i])) { kpt = kpts[i]; tpr = K / kpts[i]; return MK_OK; }
   return MK_ERR_UNSUPPORTED;
 }
 
@@ -84,7 +88,14 @@ int make_geom(int K, int rows, bool pairs, mk::GemvGeom &g) {
     if (g.RT < 1) return MK_ERR_UNSUPPORTED;
     g.RPTP = pow2_at_least((g.RT + g.NG - 1) / g.NG);
   }
-  if (g.RPTP > 16 || g.KPT * g.RPTP > 128) return MK_ERR_UNSUPPORTED;
+  if (g.RPTP > 16 || g.KPT * g.RPTP > 128) {
+    // too many rows per thread for this width: a smaller tile keeps the registers in bounds
+    while (g.RPTP > 1 && g.KPT * g.RPTP > 128) {
+      g.RPTP /= 2;
+      g.RT = pairs ? std::min(g.RT, g.RPTP * g.NG / 2) : std::min(g.RT, g.RPTP * g.NG);
+    }
+    if (g.RT < 1 || g.KPT * g.RPTP > 128) return MK_ERR_UNSUPPORTED;
+  }
   g.rows = rows;
   return MK_OK;
 }
@@ -101,6 +112,7 @@ struct mk_handle {
   int pos = 0;
   int max_chunks = 0;
   int stages = 0;
+  int ll_rep = 4;
   unsigned tag = 1;          // tag of the next forward's published activations
   size_t ll_words = 0;
   unsigned long long *ll_base = nullptr;
@@ -208,6 +220,11 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
     return fail(MK_ERR_UNSUPPORTED);
   }
   h->max_chunks = std::max(kMinChunks, h->G / Hkv);
+  // tuning knobs: copies of the tagged activation buffers (readers pick copy
+  // cta % copies, spreading the broadcast reads over more L2 lines), poll back-off
+  if (const char *e = std::getenv("MK_LL_REPLICAS")) h->ll_rep = std::max(1, std::min(16, std::atoi(e)));
+  int poll_ns = 0;
+  if (const char *e = std::getenv("MK_POLL_SLEEP_NS")) poll_ns = std::max(0, std::min(10000, std::atoi(e)));
 
   // ---- allocations ---------------------------------------------------------
   const int rope_len = c.rope_positions > 0 ? c.rope_positions : 2 * c.max_seq + 8;
@@ -223,7 +240,8 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
       (rc = h->buf.alloc((void **)&vc, kv_elems * 2)) ||
       (rc = h->buf.alloc((void **)&rope, sizeof(float2) * static_cast<size_t>(rope_len) * (d / 2))) ||
       (rc = h->buf.alloc((void **)&h->ll_base, sizeof(unsigned long long) *
-                         (h->ll_words = static_cast<size_t>(c.n_layers) * ((Hq + 2 * Hkv) * d + Hq * d + 2 * H + I)))) ||
+                         (h->ll_words = static_cast<size_t>(c.n_layers) * ((Hq + 2 * Hkv) * d + Hq * d + 2 * H + I)) *
+                         h->ll_rep)) ||
       (rc = h->buf.alloc((void **)&part, sizeof(float) * static_cast<size_t>(Hq) * h->max_chunks * (d + 2))) ||
       (rc = h->buf.alloc((void **)&cand_val, sizeof(float) * h->G)) ||
       (rc = h->buf.alloc((void **)&cand_idx, sizeof(int) * h->G)) ||
@@ -255,7 +273,7 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
       cudaMemset(tickets, 0, sizeof(unsigned) * Hkv) != cudaSuccess ||
       cudaMemset(h->d_sync, 0, sizeof(int) * 4) != cudaSuccess ||
       cudaMemset(kc, 0, kv_elems * 2) != cudaSuccess || cudaMemset(vc, 0, kv_elems * 2) != cudaSuccess ||
-      cudaMemset(h->ll_base, 0, sizeof(unsigned long long) * h->ll_words) != cudaSuccess ||
+      cudaMemset(h->ll_base, 0, sizeof(unsigned long long) * h->ll_words * h->ll_rep) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();
     return fail(MK_ERR_CUDA);
@@ -287,6 +305,9 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
     p.ll.u = q;    q += Lc * I;
     p.ll.xout = q;
   }
+  p.ll_rep = h->ll_rep;
+  p.ll_cs = h->ll_words;
+  p.poll_ns = poll_ns;
   p.part = part;
   p.cand_val = cand_val; p.cand_idx = cand_idx; p.tickets = tickets;
   p.bar = reinterpret_cast<unsigned *>(h->d_sync);
@@ -353,7 +374,7 @@ int mk_decode(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_ste
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // every forward publishes its activations under a tag never used before
   if (h->tag > 0xF0000000u - static_cast<unsigned>(n_fwd)) {
-    if (cudaMemsetAsync(h->ll_base, 0, sizeof(unsigned long long) * h->ll_words, s) != cudaSuccess) {
+    if (cudaMemsetAsync(h->ll_base, 0, sizeof(unsigned long long) * h->ll_words * h->ll_rep, s) != cudaSuccess) {
       cudaGetLastError();
       return MK_ERR_CUDA;
     }

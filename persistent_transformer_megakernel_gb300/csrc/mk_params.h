@@ -7,8 +7,13 @@
 #define MK_NCW 8
 #endif
 
+#ifndef MK_KPT_MAX
+#define MK_KPT_MAX 8
+#endif
+
 namespace mk {
 
+constexpr int KPT_MAX = MK_KPT_MAX;  // longest per-thread input slice the GEMV geometry may pick
 constexpr int NCW = MK_NCW;          // consumer warps per CTA
 constexpr int NCT = NCW * 32;        // consumer threads
 constexpr int NTHREADS = NCT + 32;   // + one TMA producer warp
@@ -65,6 +70,9 @@ struct Params {
   uint16_t *kcache, *vcache;       // [L][Hkv][max_seq][d]
   const float2 *rope;              // [rope_len][d/2] (cos, sin)
   LLBuffers ll;
+  int ll_rep;                      // copies of every tagged buffer (readers spread over them)
+  unsigned long long ll_cs;        // words between copies
+  int poll_ns;                     // back-off between unsuccessful polls
   float *part, *cand_val;
   int *cand_idx;
   unsigned *tickets;               // [Hkv]
