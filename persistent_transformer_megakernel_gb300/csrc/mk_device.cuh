@@ -203,17 +203,28 @@ __device__ __forceinline__ void ll_settle(const Params &p, SmemCtl &S, const uns
   }
 }
 
-// KPT consecutive tagged words -> floats (KPT even, src 16-byte aligned).  All
-// loads are issued at once; only words that still carry an older tag are
+// Where element k of a GEMV input vector lives in its tagged buffer.  Thread
+// kc of the consuming phase owns elements [kc*KPT, (kc+1)*KPT); they are
+// stored as KPT/2 word pairs, pair c of every thread side by side, so that
+// each of the consumer's pair loads covers consecutive 16-byte slots of
+// consecutive threads (a warp reads 512 contiguous bytes per load).
+__device__ __forceinline__ int ll_slot(const GemvGeom &g, int k) {
+  const int kc = k / g.KPT, j = k - kc * g.KPT;
+  return (j >> 1) * (2 * g.TPR) + 2 * kc + (j & 1);
+}
+
+// This thread's KPT tagged words -> floats (KPT even).  src points at the
+// thread's first pair (16-byte aligned); pair c sits at src + c * stride.
+// All loads are issued at once; only words that still carry an older tag are
 // reloaded, tracked by a bit mask.
 template <int KPT>
 __device__ __forceinline__ void ll_poll_slice(const Params &p, SmemCtl &S, const unsigned long long *src,
-                                              unsigned tag, float (&xr)[KPT]) {
+                                              int stride, unsigned tag, float (&xr)[KPT]) {
   unsigned stale = 0;
 #pragma unroll
   for (int c = 0; c < KPT / 2; ++c) {
     unsigned long long a, b;
-    ll_load2(src + 2 * c, a, b);
+    ll_load2(src + c * stride, a, b);
     xr[2 * c] = ll_val(a);
     xr[2 * c + 1] = ll_val(b);
     stale |= (ll_tag(a) != tag ? 1u : 0u) << (2 * c);
@@ -226,7 +237,7 @@ __device__ __forceinline__ void ll_poll_slice(const Params &p, SmemCtl &S, const
 #pragma unroll
     for (int j = 0; j < KPT; ++j) {
       if (stale & (1u << j)) {
-        const unsigned long long wj = ll_load(src + j);
+        const unsigned long long wj = ll_load(src + (j >> 1) * stride + (j & 1));
         if (ll_tag(wj) == tag) {
           xr[j] = ll_val(wj);
           stale &= ~(1u << j);
@@ -362,7 +373,7 @@ __device__ __forceinline__ float input_elem(const Params &p, int id, int k) {
 // Tiles are consumed without a CTA-wide barrier; row partials collect in a
 // batch buffer and one barrier per batch precedes the epilogue.
 template <int KPT, int RPTP>
-__device__ void gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer, int f,
+__device__ __noinline__ void gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer, int f,
                            int cta, int in_id, unsigned tag, uint32_t &it, int &rb, int gp) {
   const GemvGeom g = p.geo[kind];
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
@@ -390,7 +401,7 @@ __device__ void gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int
       : kind == GV_GU  ? p.ll.xmid + static_cast<size_t>(layer) * p.H
       : kind == GV_DOWN ? p.ll.u + static_cast<size_t>(layer) * p.I
                         : p.ll.xout + static_cast<size_t>(p.L - 1) * p.H;
-    ll_poll_slice<KPT>(p, S, src + (cta % p.ll_rep) * p.ll_cs + k0, tag, xr);
+    ll_poll_slice<KPT>(p, S, src + (cta % p.ll_rep) * p.ll_cs + 2 * kc, 2 * g.TPR, tag, xr);
   }
   if (norm) {
     // RMSNorm fused into the GEMV: every CTA reduces mean(x^2) itself
@@ -443,12 +454,16 @@ __device__ void gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int
       const uint32_t par = (it / static_cast<uint32_t>(p.stages)) & 1u;
       wait_full(p, S, slot, par);
       const unsigned char *st = ring + static_cast<size_t>(slot) * p.stage_bytes;
+      // every row slot computes a dot product (slots past the tile's last row
+      // re-read that row and are zeroed) so that no branch separates the rows
+      // and their load/FMA chains interleave
       float acc[RPTP];
 #pragma unroll
       for (int i = 0; i < RPTP; ++i) {
         const int row = rg + i * g.NG;
-        acc[i] = 0.f;
-        if (row < rows_in_tile) acc[i] = dot_row<KPT>(st + (static_cast<size_t>(row) * g.K + k0) * 2, xr);
+        const int rr = min(row, rows_in_tile - 1);
+        const float dv = dot_row<KPT>(st + (static_cast<size_t>(rr) * g.K + k0) * 2, xr);
+        acc[i] = row < rows_in_tile ? dv : 0.f;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[slot]);
@@ -472,23 +487,28 @@ __device__ void gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int
       if (kind == GV_GU) {
         const int base = (q / g.RT) * 2 * g.RT + (q % g.RT);
         float up = 0.f;
-        for (int ww = 0; ww < wpr; ++ww) { y += S.red[rb][base][ww]; up += S.red[rb][base + g.RT][ww]; }
-        ll_store_rep(p, p.ll.u + static_cast<size_t>(layer) * p.I + grow, y / (1.0f + expf(-y)) * up, tag);
+#pragma unroll
+        for (int ww = 0; ww < MAX_WPR; ++ww)
+          if (ww < wpr) { y += S.red[rb][base][ww]; up += S.red[rb][base + g.RT][ww]; }
+        ll_store_rep(p, p.ll.u + static_cast<size_t>(layer) * p.I + ll_slot(p.geo[GV_DOWN], grow),
+                     y / (1.0f + expf(-y)) * up, tag);
         continue;
       }
-      for (int ww = 0; ww < wpr; ++ww) y += S.red[rb][q][ww];
+#pragma unroll
+      for (int ww = 0; ww < MAX_WPR; ++ww)
+        if (ww < wpr) y += S.red[rb][q][ww];
       switch (kind) {
         case GV_QKV: ll_store_rep(p, p.ll.qkv + static_cast<size_t>(layer) * qkv_rows + grow, y, tag); break;
         case GV_O: {
           const float xn = S.xown[grow - r0] + y;
           S.xown[grow - r0] = xn;
-          ll_store_rep(p, p.ll.xmid + static_cast<size_t>(layer) * p.H + grow, xn, tag);
+          ll_store_rep(p, p.ll.xmid + static_cast<size_t>(layer) * p.H + ll_slot(p.geo[GV_GU], grow), xn, tag);
           break;
         }
         case GV_DOWN: {
           const float xn = S.xown[grow - r0] + y;
           S.xown[grow - r0] = xn;
-          ll_store_rep(p, p.ll.xout + static_cast<size_t>(layer) * p.H + grow, xn, tag);
+          ll_store_rep(p, p.ll.xout + static_cast<size_t>(layer) * p.H + ll_slot(p.geo[GV_QKV], grow), xn, tag);
           if (p.hidden) p.hidden[(static_cast<size_t>(f) * (p.L + 1) + layer + 1) * p.H + grow] = xn;
           break;
         }
@@ -514,7 +534,7 @@ __device__ void gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int
 }
 
 // dispatch on (KPT, RPTP) fixed at mk_create
-static __device__ void gemv_dispatch(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer, int f,
+static __device__ __noinline__ void gemv_dispatch(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer, int f,
                               int cta, int in_id, unsigned tag, uint32_t &it, int &rb, int gp) {
   const int kpt = p.geo[kind].KPT, r = p.geo[kind].RPTP;
 #define MK_GEMV_CASE(KP, RP) \
@@ -541,6 +561,9 @@ __device__ __forceinline__ AttnSched attn_sched(const Params &p, int f) {
   a.P = p.pos0 + f;
   a.ctx = a.P + 1;
   int cmax = p.chunks_override > 0 ? p.chunks_override : max(1, p.G / p.Hkv);
+  // short contexts: fewer, longer chunks (a chunk merge costs more than a
+  // few dozen positions of scores)
+  if (p.chunks_override <= 0 && p.attn_ppc > 0) cmax = min(cmax, (a.ctx + p.attn_ppc - 1) / p.attn_ppc);
   cmax = min(cmax, p.max_chunks);
   a.cs = (a.ctx + cmax - 1) / cmax;
   a.C = (a.ctx + a.cs - 1) / a.cs;
@@ -723,7 +746,7 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
       }
       const int j = g * GRP + h;
       if (as.C == 1) {
-        ll_store_rep(p, attn_ll + j * HD + i, os / lsum, tag);
+        ll_store_rep(p, attn_ll + ll_slot(p.geo[GV_O], j * HD + i), os / lsum, tag);
       } else {
         float *dst = p.part + (static_cast<size_t>(j) * p.max_chunks + c) * (HD + 2);
         dst[i] = os;
@@ -757,7 +780,7 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
             os = fmaf(sc, __ldcg(src + cc * (HD + 2) + i), os);
             lsum = fmaf(sc, __ldcg(src + cc * (HD + 2) + HD + 1), lsum);
           }
-          ll_store_rep(p, attn_ll + j * HD + i, os / lsum, tag);
+          ll_store_rep(p, attn_ll + ll_slot(p.geo[GV_O], j * HD + i), os / lsum, tag);
         }
       }
     }

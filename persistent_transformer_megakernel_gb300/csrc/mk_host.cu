@@ -26,6 +26,8 @@ namespace {
 
 constexpr int kStageBytes = 32 * 1024;
 constexpr int kMaxStagesWanted = 6;
+// split-KV: aim for at least this many cached positions per chunk
+constexpr int kAttnPositionsPerChunk = 64;
 constexpr int kMinChunks = 64;   // split-KV chunk capacity per kv head (at least grid / Hkv)
 
 struct DeviceBuffers {
@@ -181,6 +183,10 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
       make_geom(I, H, false, geo[mk::GV_DOWN]) ||
       make_geom(H, c.vocab, false, geo[mk::GV_LM]))
     return MK_ERR_UNSUPPORTED;
+  // the residual stream is stored in the input layout of its readers (next
+  // layer's QKV and the LM head): both must split H the same way
+  if (geo[mk::GV_LM].KPT != geo[mk::GV_QKV].KPT || geo[mk::GV_LM].TPR != geo[mk::GV_QKV].TPR)
+    return MK_ERR_UNSUPPORTED;
 
   mk_handle *h = new (std::nothrow) mk_handle();
   if (!h) return MK_ERR_NO_MEMORY;
@@ -225,6 +231,8 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
   if (const char *e = std::getenv("MK_LL_REPLICAS")) h->ll_rep = std::max(1, std::min(16, std::atoi(e)));
   int poll_ns = 0;
   if (const char *e = std::getenv("MK_POLL_SLEEP_NS")) poll_ns = std::max(0, std::min(10000, std::atoi(e)));
+  int attn_ppc = kAttnPositionsPerChunk;
+  if (const char *e = std::getenv("MK_ATTN_PPC")) attn_ppc = std::max(0, std::atoi(e));
 
   // ---- allocations ---------------------------------------------------------
   const int rope_len = c.rope_positions > 0 ? c.rope_positions : 2 * c.max_seq + 8;
@@ -308,6 +316,7 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
   p.ll_rep = h->ll_rep;
   p.ll_cs = h->ll_words;
   p.poll_ns = poll_ns;
+  p.attn_ppc = attn_ppc;
   p.part = part;
   p.cand_val = cand_val; p.cand_idx = cand_idx; p.tickets = tickets;
   p.bar = reinterpret_cast<unsigned *>(h->d_sync);

@@ -90,6 +90,7 @@ struct Params {
   float *logits, *hidden;
   unsigned long long *trace;
   int chunks_override;
+  int attn_ppc;                    // target cached positions per split-KV chunk (0: one chunk per CTA share)
   long long spin_ns;
   int fault_barrier;
   int G;                           // CTAs
