@@ -561,9 +561,10 @@ __device__ __forceinline__ AttnSched attn_sched(const Params &p, int f) {
   a.P = p.pos0 + f;
   a.ctx = a.P + 1;
   int cmax = p.chunks_override > 0 ? p.chunks_override : max(1, p.G / p.Hkv);
-  // short contexts: fewer, longer chunks (a chunk merge costs more than a
-  // few dozen positions of scores)
-  if (p.chunks_override <= 0 && p.attn_ppc > 0) cmax = min(cmax, (a.ctx + p.attn_ppc - 1) / p.attn_ppc);
+  // up to poll_cm * attn_ppc positions: poll_cm chunks (merged by polling);
+  // longer contexts: one chunk per attn_ppc positions (ticket merge)
+  if (p.chunks_override <= 0 && p.attn_ppc > 0)
+    cmax = min(cmax, max((a.ctx + p.attn_ppc - 1) / p.attn_ppc, min(p.poll_cm, a.ctx)));
   cmax = min(cmax, p.max_chunks);
   a.cs = (a.ctx + cmax - 1) / cmax;
   a.C = (a.ctx + a.cs - 1) / a.cs;
@@ -614,6 +615,67 @@ __device__ __forceinline__ void norm_rope_head(const Params &p, float (&v)[HD / 
   }
 }
 
+// Merge of split-KV chunk states for one output element (head j, dim i):
+// chunks 0..C-2 were published as tagged words (o at pc + c*cstride + i, the
+// chunk's running max m and sum l at + hd and + hd + 1); chunk C-1 is this
+// CTA's own (o_own, m_own, l_own).  All loads of a round are issued before
+// any is checked.  Returns sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c with
+// M = max_c m_c, accumulated in chunk order.
+static __device__ __noinline__ float merge_polled_chunks(const Params &p, SmemCtl &S, const unsigned long long *pc,
+                                                         size_t cstride, int hd, int i, int C, float o_own,
+                                                         float m_own, float l_own, unsigned tag) {
+  constexpr int N = MAX_POLL_CHUNKS - 1;
+  unsigned long long wo[N], wm[N], wl[N];
+#pragma unroll
+  for (int c = 0; c < N; ++c) {
+    wo[c] = wm[c] = wl[c] = static_cast<unsigned long long>(tag) << 32;
+    if (c < C - 1) {
+      wo[c] = ll_load(pc + c * cstride + i);
+      wm[c] = ll_load(pc + c * cstride + hd);
+      wl[c] = ll_load(pc + c * cstride + hd + 1);
+    }
+  }
+  Deadline dl;
+  int n = 0;
+  for (;;) {
+    bool ok = true;
+#pragma unroll
+    for (int c = 0; c < N; ++c) ok &= (ll_tag(wo[c]) == tag) & (ll_tag(wm[c]) == tag) & (ll_tag(wl[c]) == tag);
+    if (ok) break;
+#pragma unroll
+    for (int c = 0; c < N; ++c) {
+      if (ll_tag(wo[c]) != tag) wo[c] = ll_load(pc + c * cstride + i);
+      if (ll_tag(wm[c]) != tag) wm[c] = ll_load(pc + c * cstride + hd);
+      if (ll_tag(wl[c]) != tag) wl[c] = ll_load(pc + c * cstride + hd + 1);
+    }
+    if ((++n & 15) == 0) {
+      if (flag(S, F_ABORT) || ld_relaxed_i32(p.err) != 0) break;
+      if (dl.expired(p.spin_ns)) {
+        set_err(p, MK_ERR_TIMEOUT_D);
+        flag(S, F_ABORT) = 1;
+        break;
+      }
+    }
+  }
+  float M = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < N + 1; ++c)
+    if (c < C) M = fmaxf(M, c < C - 1 ? ll_val(wm[c < N ? c : 0]) : m_own);
+  float os = 0.f, lsum = 0.f;
+#pragma unroll
+  for (int c = 0; c < N + 1; ++c) {
+    if (c < C) {
+      const bool own = (c == C - 1);
+      const int k = c < N ? c : 0;
+      const float mc = own ? m_own : ll_val(wm[k]);
+      const float sc = expf(mc - M);
+      os = fmaf(sc, own ? o_own : ll_val(wo[k]), os);
+      lsum = fmaf(sc, own ? l_own : ll_val(wl[k]), lsum);
+    }
+  }
+  return os / lsum;
+}
+
 template <int HD, int GRP>
 __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring, int l, int f, int cta,
                                 unsigned tag, uint32_t &it, int gp) {
@@ -622,6 +684,8 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
   const AttnSched as = attn_sched(p, f);
   const int P = as.P;
   const int TP = p.stage_bytes / (4 * HD);     // positions per ring tile (K rows + V rows)
+  // polled merge needs every unit on its own CTA (a CTA never waits for itself)
+  const bool poll_merge = as.C > 1 && as.C <= p.poll_cm && as.units <= p.G;
   const LayerPtrs &LW = S.layers[l];
   const unsigned long long *qkv_ll = p.ll.qkv + static_cast<size_t>(l) * (p.Hq + 2 * p.Hkv) * HD +
                                      (cta % p.ll_rep) * p.ll_cs;
@@ -747,13 +811,27 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
       const int j = g * GRP + h;
       if (as.C == 1) {
         ll_store_rep(p, attn_ll + ll_slot(p.geo[GV_O], j * HD + i), os / lsum, tag);
+      } else if (poll_merge) {
+        // chunks publish (o, m, l); the chunk holding the new position merges
+        unsigned long long *pc = p.ll.part + (static_cast<size_t>(l) * MAX_POLL_CHUNKS * p.Hq + j) * (HD + 2);
+        const size_t cstride = static_cast<size_t>(p.Hq) * (HD + 2);
+        if (c < as.C - 1) {
+          ll_store(pc + c * cstride + i, os, tag);
+          if (i == 0) {
+            ll_store(pc + c * cstride + HD, M, tag);
+            ll_store(pc + c * cstride + HD + 1, lsum, tag);
+          }
+        } else {
+          const float y = merge_polled_chunks(p, S, pc, cstride, HD, i, as.C, os, M, lsum, tag);
+          ll_store_rep(p, attn_ll + ll_slot(p.geo[GV_O], j * HD + i), y, tag);
+        }
       } else {
         float *dst = p.part + (static_cast<size_t>(j) * p.max_chunks + c) * (HD + 2);
         dst[i] = os;
         if (i == 0) { dst[HD] = M; dst[HD + 1] = lsum; }
       }
     }
-    if (as.C > 1) {
+    if (as.C > 1 && !poll_merge) {
       // the last CTA to finish a chunk of kv head g merges all C chunks
       cons_sync();
       if (t == 0) {

@@ -26,8 +26,9 @@ namespace {
 
 constexpr int kStageBytes = 32 * 1024;
 constexpr int kMaxStagesWanted = 6;
-// split-KV: aim for at least this many cached positions per chunk
-constexpr int kAttnPositionsPerChunk = 64;
+// split-KV: MAX_POLL_CHUNKS chunks up to MAX_POLL_CHUNKS * this many cached
+// positions, one chunk per this many beyond
+constexpr int kAttnPositionsPerChunk = 128;
 constexpr int kMinChunks = 64;   // split-KV chunk capacity per kv head (at least grid / Hkv)
 
 struct DeviceBuffers {
@@ -248,7 +249,9 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
       (rc = h->buf.alloc((void **)&vc, kv_elems * 2)) ||
       (rc = h->buf.alloc((void **)&rope, sizeof(float2) * static_cast<size_t>(rope_len) * (d / 2))) ||
       (rc = h->buf.alloc((void **)&h->ll_base, sizeof(unsigned long long) *
-                         (h->ll_words = static_cast<size_t>(c.n_layers) * ((Hq + 2 * Hkv) * d + Hq * d + 2 * H + I)) *
+                         (h->ll_words = static_cast<size_t>(c.n_layers) *
+                                        ((Hq + 2 * Hkv) * d + Hq * d + 2 * H + I +
+                                         mk::MAX_POLL_CHUNKS * Hq * (d + 2))) *
                          h->ll_rep)) ||
       (rc = h->buf.alloc((void **)&part, sizeof(float) * static_cast<size_t>(Hq) * h->max_chunks * (d + 2))) ||
       (rc = h->buf.alloc((void **)&cand_val, sizeof(float) * h->G)) ||
@@ -311,12 +314,14 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
     p.ll.attn = q; q += Lc * Hq * d;
     p.ll.xmid = q; q += Lc * H;
     p.ll.u = q;    q += Lc * I;
-    p.ll.xout = q;
+    p.ll.xout = q; q += Lc * H;
+    p.ll.part = q;
   }
   p.ll_rep = h->ll_rep;
   p.ll_cs = h->ll_words;
   p.poll_ns = poll_ns;
   p.attn_ppc = attn_ppc;
+  p.poll_cm = mk::MAX_POLL_CHUNKS;
   p.part = part;
   p.cand_val = cand_val; p.cand_idx = cand_idx; p.tickets = tickets;
   p.bar = reinterpret_cast<unsigned *>(h->d_sync);

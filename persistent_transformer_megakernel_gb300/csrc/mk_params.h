@@ -23,6 +23,7 @@ constexpr int MAX_OWN = 64;          // residual rows one CTA may own (H / grid,
 constexpr int RED_ROWS = 64;         // rows of one GEMV epilogue batch
 constexpr int MAX_WPR = 8;           // warps that share one row (threads per row / 32)
 constexpr int MAX_GRP_HD = 256;      // group size * head_dim handled by one attention unit
+constexpr int MAX_POLL_CHUNKS = 8;    // split-KV chunk counts the chunk holding the new position merges by polling
 
 // GEMV phases in the order of their geometry table
 enum GemvKind { GV_QKV = 0, GV_O = 1, GV_GU = 2, GV_DOWN = 3, GV_LM = 4, GV_COUNT = 5 };
@@ -55,6 +56,7 @@ struct LLBuffers {
   unsigned long long *xmid;   // [L][H]               residual after attention
   unsigned long long *u;      // [L][I]               SiLU(gate) * up
   unsigned long long *xout;   // [L][H]               residual after the MLP
+  unsigned long long *part;   // [L][MAX_POLL_CHUNKS][Hq][d + 2]  chunk outputs, then running max and sum
 };
 
 struct Params {
@@ -90,6 +92,7 @@ struct Params {
   float *logits, *hidden;
   unsigned long long *trace;
   int chunks_override;
+  int poll_cm;                     // chunk counts in (1, poll_cm] merge by polling; more: ticket merge
   int attn_ppc;                    // target cached positions per split-KV chunk (0: one chunk per CTA share)
   long long spin_ns;
   int fault_barrier;
