@@ -592,26 +592,37 @@ __device__ __forceinline__ int stream_pos(const Params &p, int f, int s, int P) 
 // vector.  Lane l holds elements l + 32k so that the rotate-half partner of
 // element i (i + d/2) sits in the same lane.
 template <int HD>
-__device__ __forceinline__ void norm_rope_head(const Params &p, float (&v)[HD / 32], const uint16_t *gain,
-                                               int f, int P, bool rotate) {
+__device__ __forceinline__ void norm_rope_head(const Params &p, float (&v)[HD / 32], const float (&gain)[HD / 32],
+                                               const float2 (&cs)[HD / 64]) {
   constexpr int EPL = HD / 32;
-  const int lane = threadIdx.x & 31;
   float ss = 0.f;
 #pragma unroll
   for (int k = 0; k < EPL; ++k) ss = fmaf(v[k], v[k], ss);
   ss = warp_sum(ss);
   const float rs = 1.0f / sqrtf(ss / static_cast<float>(HD) + p.eps);
 #pragma unroll
-  for (int k = 0; k < EPL; ++k) v[k] = v[k] * rs * bf2f(gain[lane + 32 * k]);
-  if (!rotate) return;
+  for (int k = 0; k < EPL; ++k) v[k] = v[k] * rs * gain[k];
 #pragma unroll
   for (int k = 0; k < EPL / 2; ++k) {
+    const float a = v[k], b = v[k + EPL / 2];
+    v[k] = a * cs[k].x - b * cs[k].y;
+    v[k + EPL / 2] = b * cs[k].x + a * cs[k].y;
+  }
+}
+
+// the gain and rotary factors norm_rope_head needs for this lane (loaded
+// before the head vector is polled, so their latency overlaps the wait)
+template <int HD>
+__device__ __forceinline__ void norm_rope_factors(const Params &p, const uint16_t *gain, int f, int P,
+                                                  float (&g)[HD / 32], float2 (&cs)[HD / 64]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 0; k < HD / 32; ++k) g[k] = bf2f(gain[lane + 32 * k]);
+#pragma unroll
+  for (int k = 0; k < HD / 64; ++k) {
     const int i = lane + 32 * k;                         // pair index < d/2
     const int pos = stream_pos(p, f, pair_stream(p, i), P);
-    const float2 cs = p.rope[static_cast<size_t>(pos) * (HD / 2) + i];
-    const float a = v[k], b = v[k + EPL / 2];
-    v[k] = a * cs.x - b * cs.y;
-    v[k + EPL / 2] = b * cs.x + a * cs.y;
+    cs[k] = p.rope[static_cast<size_t>(pos) * (HD / 2) + i];
   }
 }
 
@@ -705,6 +716,9 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
       const unsigned long long *src = job < GRP ? qkv_ll + (g * GRP + job) * HD
                                     : job == GRP ? qkv_ll + (p.Hq + g) * HD
                                                  : qkv_ll + (p.Hq + p.Hkv + g) * HD;
+      float gv[EPL];
+      float2 csv[EPL / 2];
+      if (job <= GRP) norm_rope_factors<HD>(p, job < GRP ? LW.q_norm : LW.k_norm, f, P, gv, csv);
       unsigned long long wv[EPL];
 #pragma unroll
       for (int k = 0; k < EPL; ++k) wv[k] = ll_load(src + lane + 32 * k);
@@ -713,11 +727,11 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
 #pragma unroll
       for (int k = 0; k < EPL; ++k) v[k] = ll_val(wv[k]);
       if (job < GRP) {
-        norm_rope_head<HD>(p, v, LW.q_norm, f, P, true);
+        norm_rope_head<HD>(p, v, gv, csv);
 #pragma unroll
         for (int k = 0; k < EPL; ++k) S.qs[job * HD + lane + 32 * k] = v[k] * p.inv_sqrt_d;
       } else if (job == GRP) {
-        norm_rope_head<HD>(p, v, LW.k_norm, f, P, true);
+        norm_rope_head<HD>(p, v, gv, csv);
         uint16_t *dst = p.kcache + ((static_cast<size_t>(l) * p.Hkv + g) * p.max_seq + P) * HD;
 #pragma unroll
         for (int k = 0; k < EPL; ++k) {
@@ -1025,12 +1039,21 @@ struct Producer {
 // the kernel
 // ---------------------------------------------------------------------------
 template <int HD>
-__global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_constant__ Params pg) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   SmemCtl &S = *reinterpret_cast<SmemCtl *>(smem_raw);
   unsigned char *ring = smem_raw + RING_OFFSET;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
+  {
+    // every phase reads the launch parameters: keep them in shared memory,
+    // where a read never waits on a constant-cache refill
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(&pg);
+    uint32_t *dst = reinterpret_cast<uint32_t *>(&S.prm);
+    for (int i = tid; i < static_cast<int>(sizeof(Params) / 4); i += NTHREADS) dst[i] = src[i];
+  }
+  __syncthreads();
+  const Params &p = S.prm;
   const int NPH = 5 * p.L + 1;
 
   if (tid == 0) {

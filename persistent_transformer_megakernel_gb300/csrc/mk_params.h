@@ -108,6 +108,7 @@ enum SmemFlag { F_ABORT = 0, F_PROD_DONE = 1, F_FWD_DONE = 2, F_LAST = 3, F_COUN
 
 // static part of the dynamic shared memory; the weight ring follows at RING_OFFSET
 struct SmemCtl {
+  Params prm;                            // launch parameters, copied at kernel start
   uint64_t full[MAX_STAGES];
   uint64_t empty[MAX_STAGES];
   LayerPtrs layers[MAX_LAYERS];          // pointer table copied at kernel start
