@@ -522,6 +522,10 @@ __device__ __noinline__ void gemv_phase(const Params &p, SmemCtl &S, unsigned ch
     }
     rb ^= 1;
   }
+  // the warps without epilogue rows wait here instead of starting the next
+  // phase's polls: the publishing stores leave sooner and the poll traffic
+  // of every CTA is shorter (measured: 9% per token on the 0.6B shape)
+  cons_sync();
 
   if (kind == GV_LM) {
     block_argmax(S, best_v, best_i);
