@@ -346,8 +346,27 @@ def run_gpu(args, rank, world):
         e1.record(stream)
         e1.synchronize()
         ab_ms = e0.elapsed_time(e1)
+        # the same launches replayed from a captured graph of one forward; a
+        # first (untimed) call captures and instantiates it
+        g_ms = None
+        for timed in (False, True):
+            dec.reset()
+            if not sentinel:
+                dec.decode(d_prompt, 0, out=out)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            if sentinel:
+                dec.decode(d_prompt[:n_ab], 0, out=out, embeds=embeds, pos3=pos3[:, :n_ab].contiguous(),
+                           per_op="graph")
+            else:
+                dec.decode(None, n_ab, out=out, per_op="graph")
+            e1.record(stream)
+            e1.synchronize()
+            if timed:
+                g_ms = e0.elapsed_time(e1)
         ablation = {"us_per_token": ab_ms * 1e3 / n_ab, "forwards": n_ab,
                     "launches_per_forward": 5 * s["n_layers"] + 1,
+                    "graph_replay_us_per_token": g_ms * 1e3 / n_ab,
                     "persistent_us_per_token": total_ms * 1e3 / (n_timed * args.steps)}
 
     if rank != 0:

@@ -106,6 +106,10 @@ typedef struct {
 #define MK_DECODE_PER_OP 1u  /* run the same math as one ordinary kernel launch per
                                 phase (the launch-overhead ablation; page A, "The idea":
                                 a conventional step "launches a long chain of kernels") */
+#define MK_DECODE_PER_OP_GRAPH 2u /* the same per-phase launches, captured once per
+                                handle as a CUDA graph of one forward and replayed
+                                once per forward (the ablation without host launch
+                                cost); the first such call captures and instantiates */
 
 typedef struct {
   uint32_t flags;             /* MK_DECODE_* bits */
@@ -120,9 +124,13 @@ typedef struct {
   float *hidden;              /* device [n_in + n_steps][n_layers + 1][H] fp32 out, or NULL:
                                  the input row then the residual stream after each layer */
   uint64_t *trace;            /* device [n_fwd][5*n_layers + 1][grid][4] %globaltimer stamps
-                                 of each CTA per phase: start, input in registers, tiles
-                                 done, grid barrier passed; or NULL */
-  int32_t attn_chunks;        /* split-KV chunks per kv head; 0 = grid / n_kv_heads */
+                                 of each CTA's thread 0 per phase: start, input in
+                                 registers, tiles and epilogue done, phase left (the LM
+                                 phase: after the grid barrier that closes the forward);
+                                 or NULL */
+  int32_t attn_chunks;        /* split-KV chunks per kv head; 0 = the library's policy
+                                 (8 chunks merged by polling up to 1024 cached positions,
+                                 then one chunk per 128 positions up to grid / n_kv_heads) */
   int64_t spin_ns;            /* budget of every device wait; 0 = 1 s */
   int32_t fault_skip_barrier; /* test hook: CTA 0 skips its arrival at the grid barrier
                                  that closes forward N (0-based, persistent path only);

@@ -17,6 +17,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
 MK_DECODE_PER_OP = 1
+MK_DECODE_PER_OP_GRAPH = 2
 
 _ERRORS = {0: "ok", -1: "invalid argument", -2: "unsupported shape or launch geometry",
            -3: "KV cache full", -4: "token id or sentinel row out of range",
@@ -211,7 +212,7 @@ class Decoder:
     def _opts(self, per_op, embeds, pos3, logits, hidden, trace, attn_chunks, spin_ns,
               fault_skip_barrier):
         o = mk_decode_opts()
-        o.flags = MK_DECODE_PER_OP if per_op else 0
+        o.flags = (MK_DECODE_PER_OP_GRAPH if per_op == "graph" else MK_DECODE_PER_OP) if per_op else 0
         o.embeds = _ptr(embeds)
         o.n_embed_rows = 0 if embeds is None else embeds.shape[0]
         o.pos3 = _ptr(pos3)
@@ -224,13 +225,15 @@ class Decoder:
         return o
 
     def decode(self, in_ids=None, n_steps: int = 0, *, out: Optional[torch.Tensor] = None,
-               per_op: bool = False, embeds: Optional[torch.Tensor] = None,
+               per_op=False, embeds: Optional[torch.Tensor] = None,
                pos3: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
                hidden: Optional[torch.Tensor] = None, trace: Optional[torch.Tensor] = None,
                attn_chunks: int = 0, spin_ns: int = 0, fault_skip_barrier: int = -1,
                stream=None) -> torch.Tensor:
         """``mk_decode``: ``in_ids`` (device int32 tensor, or a sequence moved to
-        the device) then ``n_steps`` greedy forwards.  Returns the ids tensor."""
+        the device) then ``n_steps`` greedy forwards.  Returns the ids tensor.
+        ``per_op=True`` runs the one-launch-per-phase ablation, ``per_op="graph"``
+        the same launches replayed from a captured CUDA graph."""
         if in_ids is None:
             d_in = None
             n_in = 0

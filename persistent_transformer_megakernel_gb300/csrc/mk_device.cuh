@@ -1057,6 +1057,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
     for (int i = tid; i < static_cast<int>(sizeof(Params) / 4); i += NTHREADS) dst[i] = src[i];
   }
   __syncthreads();
+  if (pg.blk) {
+    // a replayed per-op graph: the call's fields live in device memory
+    if (tid == 0) {
+      const CallBlock &b = *pg.blk;
+      S.prm.in_ids = b.in_ids;
+      S.prm.out_ids = b.out_ids;
+      S.prm.embeds = b.embeds;
+      S.prm.pos3 = b.pos3;
+      S.prm.logits = b.logits;
+      S.prm.hidden = b.hidden;
+      S.prm.trace = b.trace;
+      S.prm.spin_ns = b.spin_ns;
+      S.prm.n_in = b.n_in;
+      S.prm.n_fwd = b.n_fwd;
+      S.prm.pos0 = b.pos0;
+      S.prm.n_embed_rows = b.n_embed_rows;
+      S.prm.chunks_override = b.chunks_override;
+      S.prm.op_fwd = b.op_fwd;
+      S.prm.tag0 = b.tag0;
+    }
+    __syncthreads();
+  }
   const Params &p = S.prm;
   const int NPH = 5 * p.L + 1;
 

@@ -125,7 +125,52 @@ struct mk_handle {
   mk::Params base;      // call-independent launch parameters
   int *d_sync = nullptr;       // [0] barrier counter, [1] error word, [2] last id
   int32_t *d_ids_in = nullptr, *d_ids_out = nullptr;
+  // per-op ablation under CUDA graph replay: one forward's launches, captured once
+  mk::CallBlock *d_blk = nullptr;
+  cudaStream_t cap = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t gexec = nullptr;
 };
+
+namespace {
+
+// advances the replayed graph to the next forward
+__global__ void mk_advance_forward(mk::CallBlock *b) { b->op_fwd += 1; }
+
+// capture the per-op launches of one forward (every phase, then the advance)
+int build_forward_graph(mk_handle *h) {
+  if (h->gexec) return MK_OK;
+  if (!h->cap && cudaStreamCreateWithFlags(&h->cap, cudaStreamNonBlocking) != cudaSuccess) return MK_ERR_CUDA;
+  mk::Params p = h->base;
+  p.per_op = 1;
+  p.fault_barrier = -1;
+  p.blk = h->d_blk;
+  const int nph = 5 * p.L + 1;
+  void *args[] = {&p};
+  cudaError_t e = cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeThreadLocal);
+  for (int ph = 0; ph < nph && e == cudaSuccess; ++ph) {
+    p.op_phase = ph;
+    e = cudaLaunchKernel(h->kernel, dim3(h->G), dim3(mk::NTHREADS), args, h->smem, h->cap);
+  }
+  if (e == cudaSuccess) {
+    mk_advance_forward<<<1, 1, 0, h->cap>>>(h->d_blk);
+    e = cudaGetLastError();
+  }
+  cudaGraph_t g = nullptr;
+  const cudaError_t e2 = cudaStreamEndCapture(h->cap, &g);
+  if (e == cudaSuccess) e = e2;
+  if (e == cudaSuccess) e = cudaGraphInstantiate(&h->gexec, g, 0);
+  if (e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    h->gexec = nullptr;
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
+  h->graph = g;
+  return MK_OK;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -259,7 +304,8 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
       (rc = h->buf.alloc((void **)&tickets, sizeof(unsigned) * Hkv)) ||
       (rc = h->buf.alloc((void **)&h->d_sync, sizeof(int) * 4)) ||
       (rc = h->buf.alloc((void **)&h->d_ids_in, sizeof(int32_t) * c.max_seq)) ||
-      (rc = h->buf.alloc((void **)&h->d_ids_out, sizeof(int32_t) * c.max_seq)))
+      (rc = h->buf.alloc((void **)&h->d_ids_out, sizeof(int32_t) * c.max_seq)) ||
+      (rc = h->buf.alloc((void **)&h->d_blk, sizeof(mk::CallBlock))))
     return fail(rc);
 
   std::vector<mk::LayerPtrs> lp(c.n_layers);
@@ -364,7 +410,7 @@ int mk_decode(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_ste
   o.fault_skip_barrier = -1;
   if (opts) o = *opts;
   if (o.n_embed_rows < 0 || o.attn_chunks < 0 || o.attn_chunks > h->max_chunks || o.spin_ns < 0 ||
-      (o.flags & ~MK_DECODE_PER_OP) || (o.n_embed_rows > 0 && !o.embeds))
+      (o.flags & ~(MK_DECODE_PER_OP | MK_DECODE_PER_OP_GRAPH)) || (o.n_embed_rows > 0 && !o.embeds))
     return MK_ERR_INVALID_ARG;
   if (static_cast<int64_t>(h->pos) + n_fwd > h->cfg.max_seq) return MK_ERR_KV_FULL;
   if (cudaSetDevice(h->device) != cudaSuccess) return MK_ERR_CUDA;
@@ -403,7 +449,27 @@ int mk_decode(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_ste
     return MK_ERR_CUDA;
   }
   cudaError_t e = cudaSuccess;
-  if (!(o.flags & MK_DECODE_PER_OP)) {
+  if (o.flags & MK_DECODE_PER_OP_GRAPH) {
+    // the ablation as one replay of a captured graph per forward
+    const int grc = build_forward_graph(h);
+    if (grc != MK_OK) return grc;
+    mk::CallBlock b;
+    std::memset(&b, 0, sizeof(b));
+    b.in_ids = p.in_ids; b.out_ids = p.out_ids; b.embeds = p.embeds; b.pos3 = p.pos3;
+    b.logits = p.logits; b.hidden = p.hidden; b.trace = p.trace; b.spin_ns = p.spin_ns;
+    b.n_in = p.n_in; b.n_fwd = p.n_fwd; b.pos0 = p.pos0; b.n_embed_rows = p.n_embed_rows;
+    b.chunks_override = p.chunks_override; b.op_fwd = 0; b.tag0 = p.tag0;
+    e = cudaMemcpyAsync(h->d_blk, &b, sizeof(b), cudaMemcpyHostToDevice, s);
+    for (int f = 0; f < n_fwd && e == cudaSuccess; ++f) e = cudaGraphLaunch(h->gexec, s);
+    if (e == cudaSuccess) {
+      p.per_op = 1;
+      p.fault_barrier = -1;
+      p.op_fwd = n_fwd;
+      p.op_phase = 5 * p.L + 1;   // final greedy selection
+      void *args[] = {&p};
+      e = cudaLaunchKernel(h->kernel, dim3(h->G), dim3(mk::NTHREADS), args, h->smem, s);
+    }
+  } else if (!(o.flags & MK_DECODE_PER_OP)) {
     p.per_op = 0;
     void *args[] = {&p};
     e = cudaLaunchCooperativeKernel(h->kernel, dim3(h->G), dim3(mk::NTHREADS), args, h->smem, s);
@@ -481,6 +547,9 @@ int mk_destroy(mk_handle *h) {
   if (!h) return MK_OK;
   cudaSetDevice(h->device);
   cudaDeviceSynchronize();
+  if (h->gexec) cudaGraphExecDestroy(h->gexec);
+  if (h->graph) cudaGraphDestroy(h->graph);
+  if (h->cap) cudaStreamDestroy(h->cap);
   h->buf.free_all();
   delete h;
   return MK_OK;

@@ -59,6 +59,22 @@ struct LLBuffers {
   unsigned long long *part;   // [L][MAX_POLL_CHUNKS][Hq][d + 2]  chunk outputs, then running max and sum
 };
 
+// The call-dependent launch fields.  A replayed CUDA graph of the per-op path
+// cannot change its kernels' parameters, so its launches read these from a
+// device copy the host refreshes before each call; op_fwd advances by one
+// after every forward of the graph.
+struct CallBlock {
+  const int32_t *in_ids;
+  int32_t *out_ids;
+  const float *embeds;
+  const int32_t *pos3;
+  float *logits, *hidden;
+  unsigned long long *trace;
+  long long spin_ns;
+  int n_in, n_fwd, pos0, n_embed_rows, chunks_override, op_fwd;
+  unsigned tag0;
+};
+
 struct Params {
   // shape
   int L, H, Hq, Hkv, d, I, V, vocab_in, grp;
@@ -100,6 +116,7 @@ struct Params {
   int stages, stage_bytes;
   // per-op path: one launch runs phase `op_phase` of forward `op_fwd`
   int per_op, op_fwd, op_phase;
+  const CallBlock *blk;            // per-op graph replay: call fields come from here (else NULL)
   GemvGeom geo[GV_COUNT];
 };
 

@@ -113,6 +113,23 @@ def test_per_op_path_is_bitwise_equal_to_persistent():
     assert np.array_equal(ia, ib) and np.array_equal(la, lb) and np.array_equal(ha, hb)
 
 
+def test_per_op_graph_replay_is_bitwise_equal_to_persistent():
+    # the per-op ablation replayed from a captured graph of one forward: same
+    # math, call fields read from the device call block; two calls in a row
+    # reuse the graph at a new position
+    s = W.shape("mid")
+    w = W.make_weights(s, seed=0)
+    prompt = W.make_prompt(s["vocab_in"], 6, seed=1)
+    a = mk.Decoder(s, w, max_seq=40)
+    b = mk.Decoder(s, w, max_seq=40)
+    ia, la, ha = _run_gpu(a, prompt, 10)
+    ib, lb, hb = _run_gpu(b, prompt, 10, per_op="graph")
+    assert np.array_equal(ia, ib) and np.array_equal(la, lb) and np.array_equal(ha, hb)
+    ia2, la2, ha2 = _run_gpu(a, [], 6)
+    ib2, lb2, hb2 = _run_gpu(b, [], 6, per_op="graph")
+    assert np.array_equal(ia2, ib2) and np.array_equal(la2, lb2) and np.array_equal(ha2, hb2)
+
+
 def test_repeat_runs_are_deterministic_and_reset_works():
     s = W.shape("mid")
     w = W.make_weights(s, seed=0)
