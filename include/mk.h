@@ -106,6 +106,12 @@ typedef struct {
 #define MK_DECODE_PER_OP 1u  /* run the same math as one ordinary kernel launch per
                                 phase (the launch-overhead ablation; page A, "The idea":
                                 a conventional step "launches a long chain of kernels") */
+#define MK_DECODE_STREAM 4u    /* publish each forward's greedy id to the handle's
+                                host-mapped mailbox the moment it is chosen, so the
+                                host can consume ids while the launch still runs
+                                (page A, "Porting a 1,200-line persistent CUDA
+                                megakernel...": the talker streams audio tokens out
+                                chunk by chunk); see mk_decode_start */
 #define MK_DECODE_PER_OP_GRAPH 2u /* the same per-phase launches, captured once per
                                 handle as a CUDA graph of one forward and replayed
                                 once per forward (the ablation without host launch
@@ -170,6 +176,29 @@ int mk_reset_kv(mk_handle *h, mk_stream stream);
  * mk_reset_kv.  Errors: all codes above. */
 int mk_decode(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_steps,
               int32_t *d_out_ids, const mk_decode_opts *opts, mk_stream stream);
+
+/* mk_decode without the wait: enqueue the launch on `stream` and return.  Same
+ * arguments and argument errors as mk_decode; the device status comes from
+ * mk_decode_wait, which must be called exactly once before the handle's next
+ * call (another mk_decode / mk_decode_start / mk_reset_kv first gives
+ * MK_ERR_INVALID_ARG).  With MK_DECODE_STREAM in opts->flags the mailbox is
+ * reset to zero ids before the launch and every forward's id appears in it as
+ * soon as the kernel has chosen it (mk_mailbox_read). */
+int mk_decode_start(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_steps,
+                    int32_t *d_out_ids, const mk_decode_opts *opts, mk_stream stream);
+
+/* Wait for the launch mk_decode_start enqueued; returns its status exactly as
+ * mk_decode would and advances the cursor on success.  MK_ERR_INVALID_ARG when
+ * nothing is pending. */
+int mk_decode_wait(mk_handle *h);
+
+/* Non-blocking read of the streaming mailbox: *n_out = ids the current (or last)
+ * MK_DECODE_STREAM launch has published so far -- ids 0 .. *n_out-1 of that call,
+ * each final -- and the first min(*n_out, cap) of them are copied to dst (host
+ * memory).  The mailbox is host-mapped pinned memory the handle owns (max_seq
+ * ids); the kernel writes an id, fences at system scope, then raises the count,
+ * and this read takes the count with acquire ordering before the ids. */
+int mk_mailbox_read(mk_handle *h, int32_t *dst, int32_t cap, int32_t *n_out);
 
 /* mk_decode with HOST id buffers: copies h_in_ids to the device, decodes and
  * copies the ids back to h_out_ids (n_in + n_steps entries).  The copies use

@@ -18,6 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 
 MK_DECODE_PER_OP = 1
 MK_DECODE_PER_OP_GRAPH = 2
+MK_DECODE_STREAM = 4
 
 _ERRORS = {0: "ok", -1: "invalid argument", -2: "unsupported shape or launch geometry",
            -3: "KV cache full", -4: "token id or sentinel row out of range",
@@ -64,8 +65,9 @@ class mk_info(C.Structure):
 
 
 #: every symbol include/mk.h declares
-EXPORTS = ("mk_create", "mk_reset_kv", "mk_decode", "mk_decode_host", "mk_get_info",
-           "mk_embed_sum", "mk_embed_sum_noalloc", "mk_destroy", "mk_error_string")
+EXPORTS = ("mk_create", "mk_reset_kv", "mk_decode", "mk_decode_start", "mk_decode_wait",
+           "mk_mailbox_read", "mk_decode_host", "mk_get_info", "mk_embed_sum",
+           "mk_embed_sum_noalloc", "mk_destroy", "mk_error_string")
 
 _lib = None
 
@@ -87,6 +89,9 @@ def load_library(path: Optional[str] = None):
     lib.mk_create.argtypes = [C.POINTER(mk_config), C.POINTER(mk_weights), C.POINTER(vp)]
     lib.mk_reset_kv.argtypes = [vp, vp]
     lib.mk_decode.argtypes = [vp, vp, i32, i32, vp, C.POINTER(mk_decode_opts), vp]
+    lib.mk_decode_start.argtypes = [vp, vp, i32, i32, vp, C.POINTER(mk_decode_opts), vp]
+    lib.mk_decode_wait.argtypes = [vp]
+    lib.mk_mailbox_read.argtypes = [vp, vp, i32, C.POINTER(i32)]
     lib.mk_decode_host.argtypes = [vp, vp, i32, i32, vp, C.POINTER(mk_decode_opts), vp]
     lib.mk_get_info.argtypes = [vp, C.POINTER(mk_info)]
     lib.mk_embed_sum.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, i32, vp, vp]
@@ -255,6 +260,71 @@ class Decoder:
                                 _stream_ptr(stream))
         _check(rc, "mk_decode")
         return out[:n]
+
+    def decode_start(self, in_ids=None, n_steps: int = 0, *, out: Optional[torch.Tensor] = None,
+                     stream_ids: bool = True, per_op=False, embeds: Optional[torch.Tensor] = None,
+                     pos3: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """``mk_decode_start``: enqueue the decode and return at once (with
+        ``stream_ids`` every greedy id is published to the host mailbox as it
+        is chosen).  ``decode_wait`` must follow.  Returns the device ids tensor
+        that holds all ids once the wait has returned."""
+        if in_ids is None:
+            d_in, n_in = None, 0
+        else:
+            d_in = in_ids if isinstance(in_ids, torch.Tensor) else \
+                torch.as_tensor(np.asarray(in_ids, dtype=np.int32), device=self.device)
+            d_in = d_in.to(device=self.device, dtype=torch.int32).contiguous()
+            n_in = d_in.numel()
+        n = n_in + n_steps
+        if out is None:
+            out = torch.empty(max(n, 1), dtype=torch.int32, device=self.device)
+        o = self._opts(per_op, embeds, pos3, None, None, None, 0, 0, -1)
+        if stream_ids:
+            o.flags |= MK_DECODE_STREAM
+        self._pending_keep = (d_in, out, embeds, pos3)   # alive until the wait
+        _check(self.lib.mk_decode_start(self.h, _ptr(d_in), n_in, n_steps, _ptr(out), C.byref(o),
+                                        _stream_ptr(stream)), "mk_decode_start")
+        return out[:n]
+
+    def decode_wait(self) -> None:
+        """``mk_decode_wait``: the status of the started decode."""
+        rc = self.lib.mk_decode_wait(self.h)
+        self._pending_keep = None
+        _check(rc, "mk_decode_wait")
+
+    def mailbox(self, cap: int = None) -> np.ndarray:
+        """``mk_mailbox_read``: the ids the streaming decode has published so far."""
+        cap = self.max_seq if cap is None else cap
+        buf = np.empty(max(cap, 1), dtype=np.int32)
+        n = C.c_int32(0)
+        _check(self.lib.mk_mailbox_read(self.h, buf.ctypes.data_as(C.c_void_p), cap, C.byref(n)),
+               "mk_mailbox_read")
+        return buf[:min(n.value, cap)].copy()
+
+    def decode_stream(self, in_ids=None, n_steps: int = 0, *, timeout_s: float = 60.0, **kw):
+        """Generator over ``(i, id, t)`` for every forward of a streaming
+        decode, in order, as the host sees each id appear (``t`` seconds after
+        the launch was enqueued).  The decode is waited for at the end."""
+        import time
+        n_in = 0 if in_ids is None else len(in_ids)
+        n = n_in + n_steps
+        t0 = time.perf_counter()
+        self.decode_start(in_ids, n_steps, stream_ids=True, **kw)
+        seen = 0
+        try:
+            while seen < n:
+                ids = self.mailbox(n)
+                now = time.perf_counter() - t0
+                for i in range(seen, len(ids)):
+                    yield i, int(ids[i]), now
+                seen = max(seen, len(ids))
+                if seen < n and torch.cuda.current_stream(self.device).query() and \
+                        len(self.mailbox(n)) == seen:
+                    break            # the launch ended early (an error): the wait reports it
+                if seen < n and now > timeout_s:
+                    raise RuntimeError("streaming decode: only %d of %d ids after %.0f s" % (seen, n, now))
+        finally:
+            self.decode_wait()
 
     def decode_host(self, in_ids: Sequence[int], n_steps: int = 0, *, per_op: bool = False,
                     embeds=None, pos3=None, stream=None) -> np.ndarray:

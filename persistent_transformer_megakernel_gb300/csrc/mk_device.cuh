@@ -295,6 +295,12 @@ static __device__ int select_token(const Params &p, SmemCtl &S, int f_prev, int 
   if (threadIdx.x == 0 && cta == 0) {
     p.out_ids[f_prev] = i;
     if (final) *p.last_id = i;
+    if (p.mbox_ids) {
+      // streaming: the id reaches the host's mailbox before the count does
+      *reinterpret_cast<volatile int32_t *>(p.mbox_ids + f_prev) = i;
+      __threadfence_system();
+      st_release_sys_i32(p.mbox_count, f_prev + 1);
+    }
   }
   return i;
 }
@@ -1068,6 +1074,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
       S.prm.logits = b.logits;
       S.prm.hidden = b.hidden;
       S.prm.trace = b.trace;
+      S.prm.mbox_ids = b.mbox_ids;
+      S.prm.mbox_count = b.mbox_count;
       S.prm.spin_ns = b.spin_ns;
       S.prm.n_in = b.n_in;
       S.prm.n_fwd = b.n_fwd;

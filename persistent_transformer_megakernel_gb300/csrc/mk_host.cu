@@ -125,6 +125,11 @@ struct mk_handle {
   mk::Params base;      // call-independent launch parameters
   int *d_sync = nullptr;       // [0] barrier counter, [1] error word, [2] last id
   int32_t *d_ids_in = nullptr, *d_ids_out = nullptr;
+  // streaming mailbox: host-mapped pinned ints, [0] count, ids from [32]
+  int32_t *mbox = nullptr, *d_mbox = nullptr;
+  // a launch started by mk_decode_start and not yet waited for
+  int pending = 0, pending_fwd = 0;
+  cudaStream_t pending_stream = nullptr;
   // per-op ablation under CUDA graph replay: one forward's launches, captured once
   mk::CallBlock *d_blk = nullptr;
   cudaStream_t cap = nullptr;
@@ -382,12 +387,25 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
                                3LL * H * I + 2LL * H + 2LL * d;
   h->weight_bytes = 2 * (layer_params * c.n_layers + static_cast<int64_t>(c.vocab) * H + H);
   h->kv_bytes = static_cast<int64_t>(kv_elems) * 4;
+  if (cudaHostAlloc(reinterpret_cast<void **>(&h->mbox), sizeof(int32_t) * (32 + static_cast<size_t>(c.max_seq)),
+                    cudaHostAllocMapped) != cudaSuccess) {
+    cudaGetLastError();
+    h->mbox = nullptr;
+    return fail(MK_ERR_NO_MEMORY);
+  }
+  std::memset(h->mbox, 0, sizeof(int32_t) * (32 + static_cast<size_t>(c.max_seq)));
+  if (cudaHostGetDevicePointer(reinterpret_cast<void **>(&h->d_mbox), h->mbox, 0) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFreeHost(h->mbox);
+    h->mbox = nullptr;
+    return fail(MK_ERR_CUDA);
+  }
   *out = h;
   return MK_OK;
 }
 
 int mk_reset_kv(mk_handle *h, mk_stream stream) {
-  if (!h) return MK_ERR_INVALID_ARG;
+  if (!h || h->pending) return MK_ERR_INVALID_ARG;
   h->pos = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(h->d_sync, 0, sizeof(int) * 4, s) != cudaSuccess ||
@@ -399,18 +417,24 @@ int mk_reset_kv(mk_handle *h, mk_stream stream) {
   return MK_OK;
 }
 
-int mk_decode(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_steps, int32_t *d_out_ids,
-              const mk_decode_opts *opts, mk_stream stream) {
-  if (!h || n_in < 0 || n_steps < 0) return MK_ERR_INVALID_ARG;
+int mk_decode_start(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_steps, int32_t *d_out_ids,
+                    const mk_decode_opts *opts, mk_stream stream) {
+  if (!h || h->pending || n_in < 0 || n_steps < 0) return MK_ERR_INVALID_ARG;
   const int n_fwd = n_in + n_steps;
-  if (n_fwd == 0) return MK_OK;
+  if (n_fwd == 0) {
+    h->pending = 1;
+    h->pending_fwd = 0;
+    h->pending_stream = reinterpret_cast<cudaStream_t>(stream);
+    return MK_OK;
+  }
   if (!d_out_ids || (n_in > 0 && !d_in_ids)) return MK_ERR_INVALID_ARG;
   mk_decode_opts o;
   std::memset(&o, 0, sizeof(o));
   o.fault_skip_barrier = -1;
   if (opts) o = *opts;
   if (o.n_embed_rows < 0 || o.attn_chunks < 0 || o.attn_chunks > h->max_chunks || o.spin_ns < 0 ||
-      (o.flags & ~(MK_DECODE_PER_OP | MK_DECODE_PER_OP_GRAPH)) || (o.n_embed_rows > 0 && !o.embeds))
+      (o.flags & ~(MK_DECODE_PER_OP | MK_DECODE_PER_OP_GRAPH | MK_DECODE_STREAM)) ||
+      (o.n_embed_rows > 0 && !o.embeds))
     return MK_ERR_INVALID_ARG;
   if (static_cast<int64_t>(h->pos) + n_fwd > h->cfg.max_seq) return MK_ERR_KV_FULL;
   if (cudaSetDevice(h->device) != cudaSuccess) return MK_ERR_CUDA;
@@ -430,6 +454,12 @@ int mk_decode(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_ste
   p.chunks_override = o.attn_chunks;
   p.spin_ns = o.spin_ns > 0 ? o.spin_ns : 1000000000LL;
   p.fault_barrier = o.fault_skip_barrier;
+  if (o.flags & MK_DECODE_STREAM) {
+    // an empty mailbox: the kernel raises the count as it publishes ids
+    __atomic_store_n(&h->mbox[0], 0, __ATOMIC_RELEASE);
+    p.mbox_count = h->d_mbox;
+    p.mbox_ids = h->d_mbox + 32;
+  }
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // every forward publishes its activations under a tag never used before
@@ -459,6 +489,7 @@ int mk_decode(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_ste
     b.logits = p.logits; b.hidden = p.hidden; b.trace = p.trace; b.spin_ns = p.spin_ns;
     b.n_in = p.n_in; b.n_fwd = p.n_fwd; b.pos0 = p.pos0; b.n_embed_rows = p.n_embed_rows;
     b.chunks_override = p.chunks_override; b.op_fwd = 0; b.tag0 = p.tag0;
+    b.mbox_ids = p.mbox_ids; b.mbox_count = p.mbox_count;
     e = cudaMemcpyAsync(h->d_blk, &b, sizeof(b), cudaMemcpyHostToDevice, s);
     for (int f = 0; f < n_fwd && e == cudaSuccess; ++f) e = cudaGraphLaunch(h->gexec, s);
     if (e == cudaSuccess) {
@@ -495,14 +526,42 @@ int mk_decode(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_ste
     cudaGetLastError();
     return MK_ERR_CUDA;
   }
+  h->pending = 1;
+  h->pending_fwd = n_fwd;
+  h->pending_stream = s;
+  return MK_OK;
+}
+
+int mk_decode_wait(mk_handle *h) {
+  if (!h || !h->pending) return MK_ERR_INVALID_ARG;
+  h->pending = 0;
+  if (h->pending_fwd == 0) return MK_OK;
+  cudaStream_t s = h->pending_stream;
   int herr = 0;
-  if (cudaMemcpyAsync(&herr, h->d_sync + 1, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+  if (cudaSetDevice(h->device) != cudaSuccess ||
+      cudaMemcpyAsync(&herr, h->d_sync + 1, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess) {
     cudaGetLastError();
     return MK_ERR_CUDA;
   }
   if (herr != 0) return herr;
-  h->pos += n_fwd;
+  h->pos += h->pending_fwd;
+  return MK_OK;
+}
+
+int mk_decode(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_steps, int32_t *d_out_ids,
+              const mk_decode_opts *opts, mk_stream stream) {
+  const int rc = mk_decode_start(h, d_in_ids, n_in, n_steps, d_out_ids, opts, stream);
+  if (rc != MK_OK) return rc;
+  return mk_decode_wait(h);
+}
+
+int mk_mailbox_read(mk_handle *h, int32_t *dst, int32_t cap, int32_t *n_out) {
+  if (!h || !n_out || cap < 0 || (cap > 0 && !dst)) return MK_ERR_INVALID_ARG;
+  const int32_t n = __atomic_load_n(&h->mbox[0], __ATOMIC_ACQUIRE);
+  const int32_t m = n < cap ? n : cap;
+  for (int32_t i = 0; i < m; ++i) dst[i] = __atomic_load_n(&h->mbox[32 + i], __ATOMIC_RELAXED);
+  *n_out = n;
   return MK_OK;
 }
 
@@ -550,6 +609,7 @@ int mk_destroy(mk_handle *h) {
   if (h->gexec) cudaGraphExecDestroy(h->gexec);
   if (h->graph) cudaGraphDestroy(h->graph);
   if (h->cap) cudaStreamDestroy(h->cap);
+  if (h->mbox) cudaFreeHost(h->mbox);
   h->buf.free_all();
   delete h;
   return MK_OK;

@@ -70,6 +70,8 @@ struct CallBlock {
   const int32_t *pos3;
   float *logits, *hidden;
   unsigned long long *trace;
+  int32_t *mbox_ids;
+  int *mbox_count;
   long long spin_ns;
   int n_in, n_fwd, pos0, n_embed_rows, chunks_override, op_fwd;
   unsigned tag0;
@@ -107,6 +109,8 @@ struct Params {
   const int32_t *pos3;
   float *logits, *hidden;
   unsigned long long *trace;
+  int32_t *mbox_ids;               // streaming mailbox (host-mapped), or NULL
+  int *mbox_count;
   int chunks_override;
   int poll_cm;                     // chunk counts in (1, poll_cm] merge by polling; more: ticket merge
   int attn_ppc;                    // target cached positions per split-KV chunk (0: one chunk per CTA share)

@@ -82,6 +82,10 @@ __device__ __forceinline__ int ld_relaxed_i32(const int *p) {
   return v;
 }
 // CTA-scope release/acquire on shared memory (producer <-> consumers flags)
+// release store at system scope (host-mapped memory the CPU polls)
+__device__ __forceinline__ void st_release_sys_i32(int *p, int v) {
+  asm volatile("st.release.sys.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ void st_release_cta(int *p, int v) {
   asm volatile("st.release.cta.shared.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
 }

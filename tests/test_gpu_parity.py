@@ -130,6 +130,32 @@ def test_per_op_graph_replay_is_bitwise_equal_to_persistent():
     assert np.array_equal(ia2, ib2) and np.array_equal(la2, lb2) and np.array_equal(ha2, hb2)
 
 
+def test_streaming_mailbox_publishes_every_id_while_the_launch_runs():
+    # each greedy id reaches the host-mapped mailbox as soon as it is chosen:
+    # the stream equals the ids of a plain decode, and the first id is seen
+    # before the last one exists
+    s = W.shape("mid")
+    w = W.make_weights(s, seed=0)
+    prompt = W.make_prompt(s["vocab_in"], 4, seed=1)
+    ref = mk.Decoder(s, w, max_seq=256)
+    ids_ref = ref.decode(prompt, 200).cpu().numpy()
+    dec = mk.Decoder(s, w, max_seq=256)
+    got = list(dec.decode_stream(prompt, 200))
+    assert [g[0] for g in got] == list(range(204))
+    assert np.array_equal(np.array([g[1] for g in got]), ids_ref)
+    assert got[0][2] < got[-1][2]
+    # the per-op path publishes the same stream
+    dec.reset()
+    got2 = list(dec.decode_stream(prompt, 20, per_op=True))
+    assert np.array_equal(np.array([g[1] for g in got2]), ids_ref[:24])
+    # a second start without a wait is refused; the wait then succeeds
+    dec.reset()
+    dec.decode_start(prompt, 2)
+    with pytest.raises(mk.MKError):
+        dec.decode_start(prompt, 2)
+    dec.decode_wait()
+
+
 def test_repeat_runs_are_deterministic_and_reset_works():
     s = W.shape("mid")
     w = W.make_weights(s, seed=0)
