@@ -64,23 +64,37 @@ def silu(z) -> np.ndarray:
     return z / (1.0 + np.exp(-z))
 
 
-def pair_streams(head_dim: int, mrope_sections: Optional[Sequence[int]]) -> np.ndarray:
+def pair_streams(head_dim: int, mrope_sections: Optional[Sequence[int]],
+                 interleaved: bool = False) -> np.ndarray:
     """Which position stream drives each rotary pair ``i < d/2``.
 
     Plain RoPE: stream 0 for every pair.  MRoPE (page A, "Porting it to
     Qwen3-TTS-1.7B": the talker "splits position encoding into sections"):
     contiguous runs of pair indices, ``sections[0]`` pairs on stream 0, the next
-    ``sections[1]`` on stream 1, the rest on stream 2."""
+    ``sections[1]`` on stream 1, the rest on stream 2.
+
+    Interleaved variant (the pages name only "sections"; this layout is a
+    reading): the three streams take turns pair by pair -- pair ``i`` with
+    ``i mod 3 = s`` for ``s`` in {1, 2} belongs to stream ``s`` while
+    ``i < 3 * sections[s]``; every other pair belongs to stream 0.  Each stream
+    still drives exactly ``sections[s]`` pairs."""
     half = head_dim // 2
     if mrope_sections is None:
         return np.zeros(half, dtype=np.int64)
     if sum(mrope_sections) != half:
         raise ValueError("MRoPE sections must cover head_dim/2 pairs")
-    return np.repeat(np.arange(len(mrope_sections)), mrope_sections)
+    if not interleaved:
+        return np.repeat(np.arange(len(mrope_sections)), mrope_sections)
+    out = np.zeros(half, dtype=np.int64)
+    for i in range(half):
+        r = i % 3
+        if r in (1, 2) and i < 3 * mrope_sections[r]:
+            out[i] = r
+    return out
 
 
 def rope_angles(positions, head_dim: int, theta: float,
-                mrope_sections: Optional[Sequence[int]] = None) -> np.ndarray:
+                mrope_sections: Optional[Sequence[int]] = None, interleaved: bool = False) -> np.ndarray:
     """Rotation angle of every pair: ``phi_i = pos_{s(i)} * theta^(-2i/d)``.
 
     ``positions`` is one position (plain RoPE) or three position-stream values.
@@ -91,7 +105,7 @@ def rope_angles(positions, head_dim: int, theta: float,
     i = np.arange(half, dtype=F64)
     omega = np.power(F64(theta), -2.0 * i / head_dim)
     pos = np.atleast_1d(np.asarray(positions, dtype=F64))
-    s = pair_streams(head_dim, mrope_sections)
+    s = pair_streams(head_dim, mrope_sections, interleaved)
     if pos.size == 1:
         p = np.full(half, pos[0])
     else:
@@ -178,6 +192,7 @@ class DecoderShape:
     rms_eps: float = 1e-6
     rope_theta: float = 1e6
     mrope_sections: Optional[tuple] = None
+    mrope_interleaved: bool = False
 
     @classmethod
     def from_dict(cls, s: dict) -> "DecoderShape":
@@ -188,7 +203,8 @@ class DecoderShape:
                    vocab_in=s["vocab_in"], tied=bool(s["tied"]),
                    rms_eps=float(s.get("rms_eps", 1e-6)),
                    rope_theta=float(s.get("rope_theta", 1e6)),
-                   mrope_sections=None if ms is None else tuple(ms))
+                   mrope_sections=None if ms is None else tuple(ms),
+                   mrope_interleaved=bool(s.get("mrope_interleaved", False)))
 
 
 class Weights:
@@ -251,7 +267,7 @@ class Decoder:
         pos = (P,) if pos3 is None else tuple(int(v) for v in pos3)
         if s.mrope_sections is None:
             pos = pos[:1]
-        phi = rope_angles(pos, d, s.rope_theta, s.mrope_sections)
+        phi = rope_angles(pos, d, s.rope_theta, s.mrope_sections, s.mrope_interleaved)
         x = np.asarray(x, dtype=F64).copy()
         hidden = [x.copy()]
         for l, lw in enumerate(W.layers):
@@ -325,7 +341,7 @@ def prefix_forward(shape, weight_bits: dict, tokens, sentinel_rows=None, pos3=No
     if s.mrope_sections is None:
         Phi = np.stack([rope_angles((streams[0, t],), d, s.rope_theta) for t in range(T)])
     else:
-        Phi = np.stack([rope_angles(streams[:, t], d, s.rope_theta, s.mrope_sections)
+        Phi = np.stack([rope_angles(streams[:, t], d, s.rope_theta, s.mrope_sections, s.mrope_interleaved)
                         for t in range(T)])
     Phi = Phi[:, None, :]                                   # broadcast over heads
     causal = np.triu(np.full((T, T), -np.inf), k=1)

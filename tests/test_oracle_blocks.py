@@ -166,6 +166,29 @@ def test_mrope_equal_streams_is_rope():
         assert np.array_equal(O.rope_angles(p, d, 1e6), O.rope_angles((p, p, p), d, 1e6, sec))
 
 
+def test_interleaved_mrope_layout():
+    # the interleaved reading, checked pair by pair at the talker's (24, 20, 20):
+    # streams take turns 0, 1, 2, 0, 1, 2, ... until streams 1 and 2 have their
+    # 20 pairs each (pairs 58 and 59 are the last), then pairs 60..63 are stream 0
+    d, sec = 128, (24, 20, 20)
+    st = O.decoder.pair_streams(d, sec, interleaved=True)
+    assert list(st[:9]) == [0, 1, 2, 0, 1, 2, 0, 1, 2]
+    assert list(st[56:64]) == [2, 0, 1, 2, 0, 0, 0, 0]
+    assert [int((st == k).sum()) for k in range(3)] == [24, 20, 20]
+    # equal streams reduce it to plain RoPE; a perturbed stream moves only its pairs
+    for p in (0, 7, 300):
+        assert np.array_equal(O.rope_angles(p, d, 1e6), O.rope_angles((p, p, p), d, 1e6, sec, True))
+    base = O.rope_angles((10, 10, 10), d, 1e6, sec, True)
+    for stream in range(3):
+        p3 = [10, 10, 10]
+        p3[stream] = 77
+        changed = np.nonzero(O.rope_angles(tuple(p3), d, 1e6, sec, True) != base)[0]
+        assert changed.size == sec[stream]
+        assert all(st[i] == stream for i in changed)
+    # with sections (32, 0, 0) nothing interleaves
+    assert not O.decoder.pair_streams(64, (32, 0, 0), interleaved=True).any()
+
+
 def test_mrope_sections_are_local():
     d, sec = 128, (24, 20, 20)
     base = O.rope_angles((10, 10, 10), d, 1e6, sec)

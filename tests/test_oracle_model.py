@@ -232,6 +232,24 @@ def test_mrope_model_equal_streams_and_sections():
     assert np.allclose(pl, l_d, rtol=0, atol=1e-10)
 
 
+def test_interleaved_mrope_model():
+    # equal streams: the interleaved layout is plain RoPE; distinct streams
+    # differ from the sectioned layout (other pairs take the moved angles);
+    # the prefix path follows the same interleaving
+    s, w = _tiny("mrope_small")
+    si = dict(s, mrope_interleaved=True)
+    toks = W.make_prompt(s["vocab_in"], 5, seed=1)
+    _, l_none, _ = O.Decoder(s, w, 8).generate(toks, 0)
+    _, l_ieq, _ = O.Decoder(si, w, 8).generate(toks, 0, pos3=W.make_pos3(0, 5, distinct=False))
+    assert np.array_equal(l_none, l_ieq)
+    p3 = W.make_pos3(0, 5, distinct=True)
+    _, l_sec, _ = O.Decoder(s, w, 8).generate(toks, 0, pos3=p3)
+    _, l_int, _ = O.Decoder(si, w, 8).generate(toks, 0, pos3=p3)
+    assert all(not np.allclose(l_int[t], l_sec[t]) for t in range(1, 5))
+    pl, _, _, _ = O.prefix_forward(si, w, toks, pos3=p3)
+    assert np.allclose(pl, l_int, rtol=0, atol=1e-10)
+
+
 def test_generate_feeds_back_greedy_ids():
     s, w = _tiny()
     toks = W.make_prompt(s["vocab_in"], 3, seed=1)
