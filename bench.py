@@ -327,6 +327,20 @@ def run_gpu(args, rank, world):
            "note": "mk_decode_host: prompt ids host->device, prompt + greedy forwards in one "
                    "launch, all ids device->host; host wall clock"}
 
+    # streaming: the greedy ids reach a host-mapped mailbox while the launch
+    # runs; first-id latency = enqueue to the host seeing the first greedy id
+    streaming = None
+    if not sentinel and not args.no_ablation:
+        dec.reset()
+        dec.decode(d_prompt, 0, out=out)
+        torch.cuda.synchronize()
+        n_st = min(64, n_timed)
+        got = list(dec.decode_stream(None, n_st))
+        if len(got) == n_st:
+            streaming = {"first_id_ms": got[0][2] * 1e3, "last_id_ms": got[-1][2] * 1e3, "ids": n_st,
+                         "note": "host wall clock from mk_decode_start to the id appearing in the "
+                                 "host-mapped mailbox (MK_DECODE_STREAM), greedy forwards after the prompt"}
+
     # launch-overhead ablation: the same phases as one ordinary launch each
     ablation = None
     if not args.no_ablation:
@@ -403,6 +417,8 @@ def run_gpu(args, rank, world):
         line["cpu_baseline"] = cpu
     if ablation is not None:
         line["per_op_ablation"] = ablation
+    if streaming is not None:
+        line["streaming"] = streaming
     print(json.dumps(line), flush=True)
 
 

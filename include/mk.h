@@ -61,7 +61,7 @@ typedef void *mk_stream; /* cudaStream_t */
  *   n_q_heads / n_kv_heads in {1, 2, 4, 8} and group * head_dim <= 512;
  *   every GEMV input width (hidden, n_q_heads * head_dim, intermediate) is
  *   K = KPT * T with KPT in {8, 12, 16, 24} and T in {32, 64, 128, 256};
- *   rope_mode 1 needs mrope_sections summing to head_dim / 2.             */
+ *   rope_modes 1 and 2 need mrope_sections summing to head_dim / 2.       */
 typedef struct {
   int32_t n_layers;
   int32_t hidden;          /* H */
@@ -74,7 +74,10 @@ typedef struct {
   float rms_eps;           /* RMSNorm epsilon inside the root (Qwen3: 1e-6) */
   float rope_theta;        /* rotary base (Qwen3: 1e6) */
   int32_t rope_mode;       /* 0 = RoPE, 1 = sectioned MRoPE (page A, "Porting it to
-                              Qwen3-TTS-1.7B": "splits position encoding into sections") */
+                              Qwen3-TTS-1.7B": "splits position encoding into sections"):
+                              contiguous runs of pairs per stream; 2 = interleaved MRoPE:
+                              pair i with i % 3 = s in {1, 2} follows stream s while
+                              i < 3 * mrope_sections[s], every other pair stream 0 */
   int32_t mrope_sections[3]; /* rotary pairs driven by position streams 0, 1, 2 */
   int32_t max_seq;         /* KV-cache capacity in positions */
   int32_t rope_positions;  /* rows of the host-built cos/sin table; 0 = 2*max_seq + 8
@@ -141,6 +144,23 @@ typedef struct {
   int32_t fault_skip_barrier; /* test hook: CTA 0 skips its arrival at the grid barrier
                                  that closes forward N (0-based, persistent path only);
                                  -1 = off */
+  /* Talker inputs summed inside the kernel.  When codes != NULL a negative id
+     -(r+1) selects code row r: the forward's input is
+       sum_{j<n_books} books[j][codes[r][j]] + text[text_ids[r]]
+     accumulated in fp32 in table order (codebook 0 .. n_books-1, then text) --
+     the same sum mk_embed_sum writes, so the result is bitwise that of the
+     embeds path fed by mk_embed_sum (page B, "Why Does a Single Kernel Even
+     Matter for TTS?": inputs "are sums of 17 embeddings (16 codebooks +
+     text)").  codes and embeds are exclusive.  A code or text id out of range
+     gives MK_ERR_BAD_TOKEN. */
+  const void *books;          /* device bf16 [n_books][book_rows][H] */
+  int32_t n_books;            /* 0 .. 64 */
+  int32_t book_rows;
+  const void *text;           /* device bf16 [text_rows][H] */
+  int32_t text_rows;
+  const int32_t *codes;       /* device int32 [n_code_rows][n_books] */
+  const int32_t *text_ids;    /* device int32 [n_code_rows] */
+  int32_t n_code_rows;
 } mk_decode_opts;
 
 typedef struct {

@@ -55,7 +55,10 @@ class mk_decode_opts(C.Structure):
     _fields_ = [("flags", C.c_uint32), ("embeds", C.c_void_p), ("n_embed_rows", C.c_int32),
                 ("pos3", C.c_void_p), ("logits", C.c_void_p), ("hidden", C.c_void_p),
                 ("trace", C.c_void_p), ("attn_chunks", C.c_int32), ("spin_ns", C.c_int64),
-                ("fault_skip_barrier", C.c_int32)]
+                ("fault_skip_barrier", C.c_int32),
+                ("books", C.c_void_p), ("n_books", C.c_int32), ("book_rows", C.c_int32),
+                ("text", C.c_void_p), ("text_rows", C.c_int32), ("codes", C.c_void_p),
+                ("text_ids", C.c_void_p), ("n_code_rows", C.c_int32)]
 
 
 class mk_info(C.Structure):
@@ -174,7 +177,7 @@ class Decoder:
         cfg.intermediate, cfg.vocab, cfg.vocab_in = s["intermediate"], s["vocab"], s["vocab_in"]
         cfg.rms_eps, cfg.rope_theta = s.get("rms_eps", 1e-6), s.get("rope_theta", 1e6)
         ms = s.get("mrope_sections")
-        cfg.rope_mode = 0 if ms is None else 1
+        cfg.rope_mode = 0 if ms is None else (2 if s.get("mrope_interleaved") else 1)
         if ms is not None:
             cfg.mrope_sections[0], cfg.mrope_sections[1], cfg.mrope_sections[2] = ms
         cfg.max_seq, cfg.rope_positions, cfg.flags = max_seq, rope_positions, 0
@@ -215,7 +218,7 @@ class Decoder:
 
     # ---------------------------------------------------------------- decode
     def _opts(self, per_op, embeds, pos3, logits, hidden, trace, attn_chunks, spin_ns,
-              fault_skip_barrier):
+              fault_skip_barrier, talker=None):
         o = mk_decode_opts()
         o.flags = (MK_DECODE_PER_OP_GRAPH if per_op == "graph" else MK_DECODE_PER_OP) if per_op else 0
         o.embeds = _ptr(embeds)
@@ -227,6 +230,16 @@ class Decoder:
         o.attn_chunks = attn_chunks
         o.spin_ns = spin_ns
         o.fault_skip_barrier = fault_skip_barrier
+        if talker is not None:
+            # (books bf16 [n_books][rows][H], text bf16 [rows][H], codes int32 [n][n_books], text_ids int32 [n])
+            books, text, codes, text_ids = talker
+            o.books = _ptr(books)
+            o.n_books, o.book_rows = books.shape[0], books.shape[1]
+            o.text = _ptr(text)
+            o.text_rows = text.shape[0]
+            o.codes = _ptr(codes)
+            o.text_ids = _ptr(text_ids)
+            o.n_code_rows = codes.shape[0]
         return o
 
     def decode(self, in_ids=None, n_steps: int = 0, *, out: Optional[torch.Tensor] = None,
@@ -234,11 +247,13 @@ class Decoder:
                pos3: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
                hidden: Optional[torch.Tensor] = None, trace: Optional[torch.Tensor] = None,
                attn_chunks: int = 0, spin_ns: int = 0, fault_skip_barrier: int = -1,
-               stream=None) -> torch.Tensor:
+               talker=None, stream=None) -> torch.Tensor:
         """``mk_decode``: ``in_ids`` (device int32 tensor, or a sequence moved to
         the device) then ``n_steps`` greedy forwards.  Returns the ids tensor.
         ``per_op=True`` runs the one-launch-per-phase ablation, ``per_op="graph"``
-        the same launches replayed from a captured CUDA graph."""
+        the same launches replayed from a captured CUDA graph.  ``talker`` =
+        ``(books, text, codes, text_ids)`` device tensors: negative ids select code
+        rows whose codebook + text sum the kernel forms itself."""
         if in_ids is None:
             d_in = None
             n_in = 0
@@ -254,8 +269,14 @@ class Decoder:
                       (pos3, torch.int32)):
             if t is not None and (t.dtype != dt or not t.is_cuda or not t.is_contiguous()):
                 raise ValueError("option tensors must be contiguous device tensors of the right dtype")
+        if talker is not None:
+            books, text, codes, text_ids = talker
+            if books.dtype != torch.bfloat16 or text.dtype != torch.bfloat16 or \
+                    codes.dtype != torch.int32 or text_ids.dtype != torch.int32 or \
+                    not all(t.is_cuda and t.is_contiguous() for t in talker):
+                raise ValueError("talker tables must be contiguous bf16 and ids contiguous int32 device tensors")
         o = self._opts(per_op, embeds, pos3, logits, hidden, trace, attn_chunks, spin_ns,
-                       fault_skip_barrier)
+                       fault_skip_barrier, talker)
         rc = self.lib.mk_decode(self.h, _ptr(d_in), n_in, n_steps, _ptr(out), C.byref(o),
                                 _stream_ptr(stream))
         _check(rc, "mk_decode")

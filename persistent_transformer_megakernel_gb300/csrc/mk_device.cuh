@@ -361,16 +361,53 @@ __device__ __forceinline__ float dot_row(const unsigned char *src, const float (
 
 // Input row of forward f: a non-negative id reads the embedding table, a
 // negative id -(r+1) row r of the caller's precomputed fp32 buffer (page B,
-// "Why Does a Single Kernel Even Matter for TTS?", the sentinel).
+// "Why Does a Single Kernel Even Matter for TTS?", the sentinel) -- or, with
+// code rows, the talker's sum of codebook rows and a text row, formed here in
+// fp32 in table order (codebook 0 .. n-1, then text).
 template <int KPT>
 __device__ __forceinline__ void load_input_slice(const Params &p, int id, int k0, float (&xr)[KPT]) {
-  if (id >= 0) load_bf16<KPT>(p.embed + static_cast<size_t>(id) * p.H + k0, xr);
-  else load_f32<KPT>(p.embeds + static_cast<size_t>(-id - 1) * p.H + k0, xr);
+  if (id >= 0) {
+    load_bf16<KPT>(p.embed + static_cast<size_t>(id) * p.H + k0, xr);
+  } else if (p.cb_codes) {
+    const int r = -id - 1;
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) xr[i] = 0.f;
+    for (int j = 0; j < p.cb_n; ++j) {
+      const int c = p.cb_codes[static_cast<size_t>(r) * p.cb_n + j];
+      float v[KPT];
+      load_bf16<KPT>(p.cb_books + (static_cast<size_t>(j) * p.cb_rows + c) * p.H + k0, v);
+#pragma unroll
+      for (int i = 0; i < KPT; ++i) xr[i] += v[i];
+    }
+    float v[KPT];
+    load_bf16<KPT>(p.cb_text + static_cast<size_t>(p.cb_text_ids[r]) * p.H + k0, v);
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) xr[i] += v[i];
+  } else {
+    load_f32<KPT>(p.embeds + static_cast<size_t>(-id - 1) * p.H + k0, xr);
+  }
 }
 
 __device__ __forceinline__ float input_elem(const Params &p, int id, int k) {
-  return id >= 0 ? bf2f(p.embed[static_cast<size_t>(id) * p.H + k])
-                 : p.embeds[static_cast<size_t>(-id - 1) * p.H + k];
+  if (id >= 0) return bf2f(p.embed[static_cast<size_t>(id) * p.H + k]);
+  if (!p.cb_codes) return p.embeds[static_cast<size_t>(-id - 1) * p.H + k];
+  const int r = -id - 1;
+  float acc = 0.f;
+  for (int j = 0; j < p.cb_n; ++j)
+    acc += bf2f(p.cb_books[(static_cast<size_t>(j) * p.cb_rows + p.cb_codes[static_cast<size_t>(r) * p.cb_n + j]) *
+                               p.H + k]);
+  return acc + bf2f(p.cb_text[static_cast<size_t>(p.cb_text_ids[r]) * p.H + k]);
+}
+
+// a negative id with code rows: the row and every id in it must be in range
+__device__ __forceinline__ bool code_row_ok(const Params &p, int r) {
+  if (r >= p.cb_n_rows) return false;
+  for (int j = 0; j < p.cb_n; ++j) {
+    const int c = p.cb_codes[static_cast<size_t>(r) * p.cb_n + j];
+    if (c < 0 || c >= p.cb_rows) return false;
+  }
+  const int t = p.cb_text_ids[r];
+  return t >= 0 && t < p.cb_text_rows;
 }
 
 // One GEMV phase of this CTA: y[r] = W[r,:] . in for the CTA's rows, with the
@@ -586,7 +623,11 @@ __device__ __forceinline__ AttnSched attn_sched(const Params &p, int f) {
 // sections; contiguous runs of pair indices per position stream)
 __device__ __forceinline__ int pair_stream(const Params &p, int i) {
   if (p.rope_mode == 0) return 0;
-  return i < p.sec_b0 ? 0 : (i < p.sec_b1 ? 1 : 2);
+  if (p.rope_mode == 1) return i < p.sec_b0 ? 0 : (i < p.sec_b1 ? 1 : 2);
+  // interleaved: streams take turns pair by pair until streams 1 and 2 have
+  // their sections; the remaining pairs are stream 0
+  const int r = i % 3;
+  return ((r == 1 && i < 3 * p.sec1) || (r == 2 && i < 3 * p.sec2)) ? r : 0;
 }
 
 __device__ __forceinline__ int stream_pos(const Params &p, int f, int s, int P) {
@@ -1076,6 +1117,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
       S.prm.trace = b.trace;
       S.prm.mbox_ids = b.mbox_ids;
       S.prm.mbox_count = b.mbox_count;
+      S.prm.cb_books = b.cb_books;
+      S.prm.cb_text = b.cb_text;
+      S.prm.cb_codes = b.cb_codes;
+      S.prm.cb_text_ids = b.cb_text_ids;
+      S.prm.cb_n = b.cb_n;
+      S.prm.cb_rows = b.cb_rows;
+      S.prm.cb_text_rows = b.cb_text_rows;
+      S.prm.cb_n_rows = b.cb_n_rows;
       S.prm.spin_ns = b.spin_ns;
       S.prm.n_in = b.n_in;
       S.prm.n_fwd = b.n_fwd;
@@ -1174,7 +1223,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
         else if (f > 0) id = prev;
         else id = *p.last_id;
         const bool bad = (id >= 0) ? (id >= p.vocab_in)
-                                   : (p.embeds == nullptr || -(id + 1) >= p.n_embed_rows);
+                       : p.cb_codes ? !code_row_ok(p, -(id + 1))
+                                    : (p.embeds == nullptr || -(id + 1) >= p.n_embed_rows);
         if (bad) {
           if (tid == 0) set_err(p, MK_ERR_BAD_TOKEN_D);
           ok = false;

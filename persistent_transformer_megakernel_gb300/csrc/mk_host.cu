@@ -209,8 +209,8 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
   if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return MK_ERR_UNSUPPORTED;
   if (grp * c.head_dim > mk::MAX_GRP_HD) return MK_ERR_UNSUPPORTED;
   if (c.n_layers > mk::MAX_LAYERS) return MK_ERR_UNSUPPORTED;
-  if (c.rope_mode != 0 && c.rope_mode != 1) return MK_ERR_INVALID_ARG;
-  if (c.rope_mode == 1) {
+  if (c.rope_mode < 0 || c.rope_mode > 2) return MK_ERR_INVALID_ARG;
+  if (c.rope_mode != 0) {
     if (c.mrope_sections[0] < 0 || c.mrope_sections[1] < 0 || c.mrope_sections[2] < 0 ||
         c.mrope_sections[0] + c.mrope_sections[1] + c.mrope_sections[2] != c.head_dim / 2)
       return MK_ERR_INVALID_ARG;
@@ -350,6 +350,8 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
   p.rope_mode = c.rope_mode;
   p.sec_b0 = c.rope_mode ? c.mrope_sections[0] : d / 2;
   p.sec_b1 = c.rope_mode ? c.mrope_sections[0] + c.mrope_sections[1] : d / 2;
+  p.sec1 = c.rope_mode ? c.mrope_sections[1] : 0;
+  p.sec2 = c.rope_mode ? c.mrope_sections[2] : 0;
   p.max_seq = c.max_seq;
   p.rope_len = rope_len;
   p.max_chunks = h->max_chunks;
@@ -436,6 +438,9 @@ int mk_decode_start(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t
       (o.flags & ~(MK_DECODE_PER_OP | MK_DECODE_PER_OP_GRAPH | MK_DECODE_STREAM)) ||
       (o.n_embed_rows > 0 && !o.embeds))
     return MK_ERR_INVALID_ARG;
+  if (o.codes && (o.embeds || o.n_books < 0 || o.n_books > 64 || (o.n_books > 0 && (!o.books || o.book_rows < 1)) ||
+                  !o.text || o.text_rows < 1 || !o.text_ids || o.n_code_rows < 0))
+    return MK_ERR_INVALID_ARG;
   if (static_cast<int64_t>(h->pos) + n_fwd > h->cfg.max_seq) return MK_ERR_KV_FULL;
   if (cudaSetDevice(h->device) != cudaSuccess) return MK_ERR_CUDA;
 
@@ -454,6 +459,16 @@ int mk_decode_start(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t
   p.chunks_override = o.attn_chunks;
   p.spin_ns = o.spin_ns > 0 ? o.spin_ns : 1000000000LL;
   p.fault_barrier = o.fault_skip_barrier;
+  if (o.codes) {
+    p.cb_books = static_cast<const uint16_t *>(o.books);
+    p.cb_text = static_cast<const uint16_t *>(o.text);
+    p.cb_codes = o.codes;
+    p.cb_text_ids = o.text_ids;
+    p.cb_n = o.n_books;
+    p.cb_rows = o.book_rows;
+    p.cb_text_rows = o.text_rows;
+    p.cb_n_rows = o.n_code_rows;
+  }
   if (o.flags & MK_DECODE_STREAM) {
     // an empty mailbox: the kernel raises the count as it publishes ids
     __atomic_store_n(&h->mbox[0], 0, __ATOMIC_RELEASE);
@@ -490,6 +505,8 @@ int mk_decode_start(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t
     b.n_in = p.n_in; b.n_fwd = p.n_fwd; b.pos0 = p.pos0; b.n_embed_rows = p.n_embed_rows;
     b.chunks_override = p.chunks_override; b.op_fwd = 0; b.tag0 = p.tag0;
     b.mbox_ids = p.mbox_ids; b.mbox_count = p.mbox_count;
+    b.cb_books = p.cb_books; b.cb_text = p.cb_text; b.cb_codes = p.cb_codes; b.cb_text_ids = p.cb_text_ids;
+    b.cb_n = p.cb_n; b.cb_rows = p.cb_rows; b.cb_text_rows = p.cb_text_rows; b.cb_n_rows = p.cb_n_rows;
     e = cudaMemcpyAsync(h->d_blk, &b, sizeof(b), cudaMemcpyHostToDevice, s);
     for (int f = 0; f < n_fwd && e == cudaSuccess; ++f) e = cudaGraphLaunch(h->gexec, s);
     if (e == cudaSuccess) {

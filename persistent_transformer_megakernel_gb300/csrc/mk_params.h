@@ -73,6 +73,9 @@ struct CallBlock {
   int32_t *mbox_ids;
   int *mbox_count;
   long long spin_ns;
+  const uint16_t *cb_books, *cb_text;
+  const int32_t *cb_codes, *cb_text_ids;
+  int cb_n, cb_rows, cb_text_rows, cb_n_rows;
   int n_in, n_fwd, pos0, n_embed_rows, chunks_override, op_fwd;
   unsigned tag0;
 };
@@ -81,7 +84,8 @@ struct Params {
   // shape
   int L, H, Hq, Hkv, d, I, V, vocab_in, grp;
   float eps, inv_sqrt_d;
-  int rope_mode, sec_b0, sec_b1;   // pair i < sec_b0 -> stream 0, < sec_b1 -> 1, else 2
+  int rope_mode, sec_b0, sec_b1;   // mode 2 (interleaved) uses sec1, sec2
+  int sec1, sec2;   // pair i < sec_b0 -> stream 0, < sec_b1 -> 1, else 2
   int max_seq, rope_len, max_chunks;
   // weights (borrowed)
   const LayerPtrs *layers;
@@ -111,6 +115,10 @@ struct Params {
   unsigned long long *trace;
   int32_t *mbox_ids;               // streaming mailbox (host-mapped), or NULL
   int *mbox_count;
+  // talker inputs summed in-kernel (negative ids select code rows), or cb_codes NULL
+  const uint16_t *cb_books, *cb_text;
+  const int32_t *cb_codes, *cb_text_ids;
+  int cb_n, cb_rows, cb_text_rows, cb_n_rows;
   int chunks_override;
   int poll_cm;                     // chunk counts in (1, poll_cm] merge by polling; more: ticket merge
   int attn_ppc;                    // target cached positions per split-KV chunk (0: one chunk per CTA share)

@@ -20,14 +20,14 @@ pytestmark = pytest.mark.gpu
 mk = pytest.importorskip("persistent_transformer_megakernel_gb300")
 
 
-def _run_gpu(dec, feed, n_steps=0, embeds=None, pos3=None, per_op=False, attn_chunks=0):
+def _run_gpu(dec, feed, n_steps=0, embeds=None, pos3=None, per_op=False, attn_chunks=0, talker=None):
     s = dec.shape
     n = len(feed) + n_steps
     logits = torch.full((n, s["vocab"]), float("nan"), dtype=torch.float32, device="cuda:0")
     hidden = torch.full((n, s["n_layers"] + 1, s["hidden"]), float("nan"), dtype=torch.float32,
                         device="cuda:0")
     ids = dec.decode(feed, n_steps, logits=logits, hidden=hidden, embeds=embeds, pos3=pos3,
-                     per_op=per_op, attn_chunks=attn_chunks)
+                     per_op=per_op, attn_chunks=attn_chunks, talker=talker)
     torch.cuda.synchronize()
     return ids.cpu().numpy(), logits.double().cpu().numpy(), hidden.double().cpu().numpy()
 
@@ -65,6 +65,11 @@ def test_teacher_forced_parity(name, n_prompt, n_steps):
 @pytest.mark.parametrize("mode", ["equal", "distinct"])
 def test_mrope_parity(mode):
     _teacher_forced("mrope_small", 6, 10, max_seq=24, pos3_mode=mode)
+
+
+def test_interleaved_mrope_parity():
+    # streams taking turns pair by pair (rope_mode 2), distinct position streams
+    _teacher_forced("mrope_small_interleaved", 6, 10, max_seq=24, pos3_mode="distinct")
 
 
 def test_free_running_greedy_matches_until_a_near_tie():
@@ -128,6 +133,41 @@ def test_per_op_graph_replay_is_bitwise_equal_to_persistent():
     ia2, la2, ha2 = _run_gpu(a, [], 6)
     ib2, lb2, hb2 = _run_gpu(b, [], 6, per_op="graph")
     assert np.array_equal(ia2, ib2) and np.array_equal(la2, lb2) and np.array_equal(ha2, hb2)
+
+
+def test_in_kernel_talker_sum_equals_the_sentinel_buffer_path():
+    # negative ids with code rows: the kernel sums 16 codebook rows and a text
+    # row itself, in the order mk_embed_sum uses -> bitwise the same forwards
+    s = W.shape("mrope_small")
+    w = W.make_weights(s, seed=0)
+    n = 12
+    tables = W.make_tts_tables(s["hidden"], seed=3)
+    codes, text = W.make_tts_codes(n, seed=2)
+    books = torch.from_numpy(tables["codebooks"].view(np.int16)).view(torch.bfloat16).cuda()
+    txt = torch.from_numpy(tables["text"].view(np.int16)).view(torch.bfloat16).cuda()
+    codes_d = torch.as_tensor(codes, dtype=torch.int32).cuda().contiguous()
+    text_d = torch.as_tensor(text, dtype=torch.int32).cuda().contiguous()
+    E = mk.embed_sum(books, txt, codes_d, text_d)
+    sid = W.sentinel_ids(n)
+    pos3 = torch.as_tensor(W.make_pos3(0, n, distinct=True), dtype=torch.int32).cuda().contiguous()
+    a = mk.Decoder(s, w, max_seq=32)
+    ia, la, ha = _run_gpu(a, sid, 3, embeds=E, pos3=None)
+    b = mk.Decoder(s, w, max_seq=32)
+    ib, lb, hb = _run_gpu(b, sid, 3, talker=(books, txt, codes_d, text_d))
+    assert np.array_equal(ia, ib) and np.array_equal(la, lb) and np.array_equal(ha, hb)
+    # distinct MRoPE streams too, through the per-op path
+    a.reset(); b.reset()
+    p3 = torch.as_tensor(W.make_pos3(0, n, distinct=True), dtype=torch.int32).cuda().contiguous()
+    ia, la, ha = _run_gpu(a, sid, 0, embeds=E, pos3=p3)
+    ib, lb, hb = _run_gpu(b, sid, 0, pos3=p3, per_op=True, talker=(books, txt, codes_d, text_d))
+    assert np.array_equal(ia, ib) and np.array_equal(la, lb) and np.array_equal(ha, hb)
+    # a code out of range is a bad token, reported without a fault
+    bad = codes_d.clone()
+    bad[5, 3] = books.shape[1]
+    c = mk.Decoder(s, w, max_seq=32)
+    with pytest.raises(mk.MKError):
+        _run_gpu(c, sid, 0, talker=(books, txt, bad, text_d))
+    del pos3
 
 
 def test_streaming_mailbox_publishes_every_id_while_the_launch_runs():

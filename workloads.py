@@ -63,6 +63,10 @@ SHAPES = {
     "mrope_small": dict(n_layers=2, hidden=512, n_q_heads=8, n_kv_heads=4, head_dim=64,
                         intermediate=1536, vocab=1024, vocab_in=1024, tied=False,
                         mrope_sections=(12, 10, 10)),
+    # the same with the interleaved MRoPE layout
+    "mrope_small_interleaved": dict(n_layers=2, hidden=512, n_q_heads=8, n_kv_heads=4, head_dim=64,
+                                    intermediate=1536, vocab=1024, vocab_in=1024, tied=False,
+                                    mrope_sections=(12, 10, 10), mrope_interleaved=True),
 }
 
 #: fixed scalars of every shape (Qwen3 defaults)
