@@ -336,10 +336,24 @@ def run_gpu(args, rank, world):
         torch.cuda.synchronize()
         n_st = min(64, n_timed)
         got = list(dec.decode_stream(None, n_st))
+        # time to first token from a cold context: host prompt ids in, the
+        # prompt consumed one token per forward, the first generated id read
+        # from the mailbox (host wall clock)
+        dec.reset()
+        torch.cuda.synchronize()
+        host_prompt = [int(t) for t in prompt]
+        first = None
+        for i, tok, t in dec.decode_stream(host_prompt, 1):
+            if i == len(host_prompt) - 1:
+                first = t
         if len(got) == n_st:
             streaming = {"first_id_ms": got[0][2] * 1e3, "last_id_ms": got[-1][2] * 1e3, "ids": n_st,
+                         "ttft_ms": None if first is None else first * 1e3,
+                         "ttft_prompt": len(host_prompt),
                          "note": "host wall clock from mk_decode_start to the id appearing in the "
-                                 "host-mapped mailbox (MK_DECODE_STREAM), greedy forwards after the prompt"}
+                                 "host-mapped mailbox (MK_DECODE_STREAM); first_id/last_id: greedy forwards "
+                                 "after a resident prompt; ttft: a %d-token host prompt consumed one token per "
+                                 "forward in the same launch, to the first generated id" % len(host_prompt)}
 
     # launch-overhead ablation: the same phases as one ordinary launch each
     ablation = None

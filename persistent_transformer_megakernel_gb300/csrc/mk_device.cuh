@@ -524,7 +524,8 @@ __device__ __noinline__ void gemv_phase(const Params &p, SmemCtl &S, unsigned ch
     // ---- epilogue of the batch: one thread per output row (pair) ------------
     const int a0 = r0 + tb * g.RT;
     const int nout = min(r1, r0 + te * g.RT) - a0;
-    for (int q = t; q < nout; q += NCT) {
+    // rows go to warps 1.. first: warp 0 shares its scheduler with the producer warp
+    for (int q = (t + NCT - 32) % NCT; q < nout; q += NCT) {
       const int grow = a0 + q;
       float y = 0.f;
       if (kind == GV_GU) {

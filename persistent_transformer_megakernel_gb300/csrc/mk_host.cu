@@ -115,7 +115,7 @@ struct mk_handle {
   int pos = 0;
   int max_chunks = 0;
   int stages = 0;
-  int ll_rep = 4;
+  int ll_rep = 1;             // copies of every tagged buffer (MK_LL_REPLICAS); one measured fastest
   unsigned tag = 1;          // tag of the next forward's published activations
   size_t ll_words = 0;
   unsigned long long *ll_base = nullptr;
