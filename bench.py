@@ -346,14 +346,27 @@ def run_gpu(args, rank, world):
         for i, tok, t in dec.decode_stream(host_prompt, 1):
             if i == len(host_prompt) - 1:
                 first = t
+        # the same with the batched prefill (tensor-core GEMMs for the prompt):
+        # host ids in, prefill, the first generated id back on the host
+        pf_ms = []
+        for rep in range(4):
+            dec.reset()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            first_id = int(dec.prefill(host_prompt)[-1].item())
+            pf_ms.append((time.perf_counter() - t0) * 1e3)
+        del first_id
         if len(got) == n_st:
             streaming = {"first_id_ms": got[0][2] * 1e3, "last_id_ms": got[-1][2] * 1e3, "ids": n_st,
                          "ttft_ms": None if first is None else first * 1e3,
+                         "ttft_prefill_ms": min(pf_ms[1:]),
                          "ttft_prompt": len(host_prompt),
                          "note": "host wall clock from mk_decode_start to the id appearing in the "
                                  "host-mapped mailbox (MK_DECODE_STREAM); first_id/last_id: greedy forwards "
                                  "after a resident prompt; ttft: a %d-token host prompt consumed one token per "
-                                 "forward in the same launch, to the first generated id" % len(host_prompt)}
+                                 "forward in the same launch, to the first generated id; ttft_prefill: the "
+                                 "same prompt through mk_prefill (batched tensor-core GEMMs), best of 3 after "
+                                 "a first call that allocates the scratch" % len(host_prompt)}
 
     # launch-overhead ablation: the same phases as one ordinary launch each
     ablation = None

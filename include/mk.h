@@ -197,6 +197,29 @@ int mk_reset_kv(mk_handle *h, mk_stream stream);
 int mk_decode(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_steps,
               int32_t *d_out_ids, const mk_decode_opts *opts, mk_stream stream);
 
+/* Batched prompt prefill: the n forwards of mk_decode(h, d_in_ids, n, 0, ...)
+ * computed all at once per layer instead of one token per forward -- the
+ * projections as bf16 tensor-core GEMMs with fp32 accumulation (each fp32
+ * activation enters as three bf16 terms, hi + mid + lo: all 24 bits), then
+ * QK-norm, RoPE / MRoPE,
+ * the bf16 KV append and causal attention over the cache in the library's own
+ * kernels.  It fills the same KV cache and advances the same cursor, so a
+ * following mk_decode(h, NULL, 0, n_steps, ...) continues from the prompt's
+ * greedy id (page A, "Porting a 1,200-line persistent CUDA megakernel to
+ * Qwen3-TTS": the time to the first chunk is what the listener waits for).
+ *   d_in_ids: device int32 [n] (negative ids pick rows of opts->embeds).
+ *   d_out_ids: device int32 [n] greedy ids after every prompt token, or NULL
+ *   (then only the last token's logits are computed).  opts: embeds, pos3,
+ *   logits ([n][vocab]) and hidden ([n][L+1][H]) as for mk_decode; flags,
+ *   trace and code rows must be unset.  Not bitwise equal to mk_decode (other
+ *   summation orders); both follow the oracle within the parity tolerance.
+ * Blocks until `stream` completes.  Errors: MK_ERR_INVALID_ARG, MK_ERR_KV_FULL,
+ * MK_ERR_BAD_TOKEN, MK_ERR_BAD_POSITION, MK_ERR_NUMERIC, MK_ERR_NO_MEMORY
+ * (scratch for 256 tokens is allocated on the first call), MK_ERR_UNSUPPORTED,
+ * MK_ERR_CUDA. */
+int mk_prefill(mk_handle *h, const int32_t *d_in_ids, int32_t n, int32_t *d_out_ids,
+               const mk_decode_opts *opts, mk_stream stream);
+
 /* mk_decode without the wait: enqueue the launch on `stream` and return.  Same
  * arguments and argument errors as mk_decode; the device status comes from
  * mk_decode_wait, which must be called exactly once before the handle's next

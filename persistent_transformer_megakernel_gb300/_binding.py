@@ -68,7 +68,7 @@ class mk_info(C.Structure):
 
 
 #: every symbol include/mk.h declares
-EXPORTS = ("mk_create", "mk_reset_kv", "mk_decode", "mk_decode_start", "mk_decode_wait",
+EXPORTS = ("mk_create", "mk_reset_kv", "mk_decode", "mk_prefill", "mk_decode_start", "mk_decode_wait",
            "mk_mailbox_read", "mk_decode_host", "mk_get_info", "mk_embed_sum",
            "mk_embed_sum_noalloc", "mk_destroy", "mk_error_string")
 
@@ -92,6 +92,7 @@ def load_library(path: Optional[str] = None):
     lib.mk_create.argtypes = [C.POINTER(mk_config), C.POINTER(mk_weights), C.POINTER(vp)]
     lib.mk_reset_kv.argtypes = [vp, vp]
     lib.mk_decode.argtypes = [vp, vp, i32, i32, vp, C.POINTER(mk_decode_opts), vp]
+    lib.mk_prefill.argtypes = [vp, vp, i32, vp, C.POINTER(mk_decode_opts), vp]
     lib.mk_decode_start.argtypes = [vp, vp, i32, i32, vp, C.POINTER(mk_decode_opts), vp]
     lib.mk_decode_wait.argtypes = [vp]
     lib.mk_mailbox_read.argtypes = [vp, vp, i32, C.POINTER(i32)]
@@ -281,6 +282,25 @@ class Decoder:
                                 _stream_ptr(stream))
         _check(rc, "mk_decode")
         return out[:n]
+
+    def prefill(self, in_ids, *, out: Optional[torch.Tensor] = None, all_ids: bool = True,
+                embeds: Optional[torch.Tensor] = None, pos3: Optional[torch.Tensor] = None,
+                logits: Optional[torch.Tensor] = None, hidden: Optional[torch.Tensor] = None,
+                stream=None) -> Optional[torch.Tensor]:
+        """``mk_prefill``: the prompt's forwards as batched tensor-core GEMMs.
+        Returns the greedy id after every prompt token (``all_ids``) or None
+        (then only the last token's logits are computed; the next ``decode``
+        continues from its id)."""
+        d_in = in_ids if isinstance(in_ids, torch.Tensor) else \
+            torch.as_tensor(np.asarray(in_ids, dtype=np.int32), device=self.device)
+        d_in = d_in.to(device=self.device, dtype=torch.int32).contiguous()
+        n = d_in.numel()
+        if all_ids and out is None:
+            out = torch.empty(max(n, 1), dtype=torch.int32, device=self.device)
+        o = self._opts(False, embeds, pos3, logits, hidden, None, 0, 0, -1)
+        _check(self.lib.mk_prefill(self.h, _ptr(d_in), n, _ptr(out) if all_ids else None, C.byref(o),
+                                   _stream_ptr(stream)), "mk_prefill")
+        return out[:n] if all_ids else None
 
     def decode_start(self, in_ids=None, n_steps: int = 0, *, out: Optional[torch.Tensor] = None,
                      stream_ids: bool = True, per_op=False, embeds: Optional[torch.Tensor] = None,

@@ -20,6 +20,7 @@
 
 #include "../../include/mk.h"
 #include "mk_launch.h"
+#include "mk_prefill.h"
 #include "mk_params.h"
 
 namespace {
@@ -125,6 +126,9 @@ struct mk_handle {
   mk::Params base;      // call-independent launch parameters
   int *d_sync = nullptr;       // [0] barrier counter, [1] error word, [2] last id
   int32_t *d_ids_in = nullptr, *d_ids_out = nullptr;
+  // batched prompt prefill: host copy of the layer pointers, scratch, GEMM handle
+  std::vector<mkp::PfLayer> pf_layers;
+  mkp::PfState pf;
   // streaming mailbox: host-mapped pinned ints, [0] count, ids from [32]
   int32_t *mbox = nullptr, *d_mbox = nullptr;
   // a launch started by mk_decode_start and not yet waited for
@@ -321,6 +325,10 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
                           (const uint16_t *)L.wo, (const uint16_t *)L.mlp_norm, (const uint16_t *)L.w_gate,
                           (const uint16_t *)L.w_up, (const uint16_t *)L.w_down};
   }
+  h->pf_layers.resize(c.n_layers);
+  for (int l = 0; l < c.n_layers; ++l)
+    h->pf_layers[l] = mkp::PfLayer{lp[l].attn_norm, lp[l].wq, lp[l].wk, lp[l].wv, lp[l].q_norm, lp[l].k_norm,
+                                   lp[l].wo, lp[l].mlp_norm, lp[l].w_gate, lp[l].w_up, lp[l].w_down};
   // rotary table: cos/sin(pos * theta^(-2i/d)) evaluated in double
   std::vector<float2> tab(static_cast<size_t>(rope_len) * (d / 2));
   for (int pos = 0; pos < rope_len; ++pos)
@@ -573,6 +581,39 @@ int mk_decode(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_ste
   return mk_decode_wait(h);
 }
 
+int mk_prefill(mk_handle *h, const int32_t *d_in_ids, int32_t n, int32_t *d_out_ids, const mk_decode_opts *opts,
+               mk_stream stream) {
+  if (!h || h->pending || n < 0) return MK_ERR_INVALID_ARG;
+  if (n == 0) return MK_OK;
+  if (!d_in_ids) return MK_ERR_INVALID_ARG;
+  mk_decode_opts o;
+  std::memset(&o, 0, sizeof(o));
+  if (opts) o = *opts;
+  if (o.flags || o.trace || o.codes || o.n_embed_rows < 0 || (o.n_embed_rows > 0 && !o.embeds))
+    return MK_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(h->pos) + n > h->cfg.max_seq) return MK_ERR_KV_FULL;
+  if (cudaSetDevice(h->device) != cudaSuccess) return MK_ERR_CUDA;
+  const mk_config &c = h->cfg;
+  int rc = mkp::pf_init(h->pf, std::min(256, c.max_seq), c.hidden, c.n_q_heads, c.n_kv_heads, c.head_dim,
+                        c.intermediate);
+  if (rc != MK_OK) return rc;
+  const mk::Params &p = h->base;
+  mkp::PfArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.L = p.L; a.H = p.H; a.Hq = p.Hq; a.Hkv = p.Hkv; a.d = p.d; a.I = p.I; a.V = p.V; a.vocab_in = p.vocab_in;
+  a.eps = p.eps; a.inv_sqrt_d = p.inv_sqrt_d;
+  a.rope_mode = p.rope_mode; a.sec0 = p.sec_b0; a.sec1 = p.sec1; a.sec2 = p.sec2;
+  a.rope_len = p.rope_len; a.max_seq = p.max_seq;
+  a.embed = p.embed; a.rope = p.rope; a.kcache = p.kcache; a.vcache = p.vcache;
+  a.ids = d_in_ids; a.embeds = o.embeds; a.n_embed_rows = o.embeds ? o.n_embed_rows : 0;
+  a.pos3 = o.pos3; a.n_pos = n; a.pos0 = h->pos; a.hidden = o.hidden;
+  rc = mkp::pf_run(h->pf, a, h->pf_layers.data(), p.final_norm, p.lm_head, n, d_out_ids, o.logits, p.last_id,
+                   reinterpret_cast<cudaStream_t>(stream));
+  if (rc != MK_OK) return rc;
+  h->pos += n;
+  return MK_OK;
+}
+
 int mk_mailbox_read(mk_handle *h, int32_t *dst, int32_t cap, int32_t *n_out) {
   if (!h || !n_out || cap < 0 || (cap > 0 && !dst)) return MK_ERR_INVALID_ARG;
   const int32_t n = __atomic_load_n(&h->mbox[0], __ATOMIC_ACQUIRE);
@@ -627,6 +668,7 @@ int mk_destroy(mk_handle *h) {
   if (h->graph) cudaGraphDestroy(h->graph);
   if (h->cap) cudaStreamDestroy(h->cap);
   if (h->mbox) cudaFreeHost(h->mbox);
+  mkp::pf_free(h->pf);
   h->buf.free_all();
   delete h;
   return MK_OK;

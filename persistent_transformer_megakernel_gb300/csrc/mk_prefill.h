@@ -1,0 +1,60 @@
+// Batched prompt prefill (csrc/mk_prefill.cu): interface between the C ABI in
+// mk_host.cu and the prefill kernels + tensor-core GEMMs.
+#pragma once
+#include <cstdint>
+#include <cstddef>
+#include <cuda_runtime.h>
+
+#include "../../include/mk.h"
+
+namespace mkp {
+
+constexpr int MK_PF_ERR_BAD_TOKEN = MK_ERR_BAD_TOKEN;
+constexpr int MK_PF_ERR_NUMERIC = MK_ERR_NUMERIC;
+constexpr int MK_PF_ERR_BAD_POSITION = MK_ERR_BAD_POSITION;
+
+// everything a prefill kernel reads: shape, model, handle state, call, scratch
+struct PfArgs {
+  int L, H, Hq, Hkv, d, I, V, vocab_in;
+  float eps, inv_sqrt_d;
+  int rope_mode, sec0, sec1, sec2, rope_len, max_seq;
+  const uint16_t *embed;            // [vocab_in][H] bf16
+  const float2 *rope;               // [rope_len][d/2] (cos, sin)
+  uint16_t *kcache, *vcache;        // [L][Hkv][max_seq][d] bf16, the decode kernel's cache
+  const int32_t *ids;               // [n] prompt ids (device)
+  const float *embeds;              // sentinel rows [n_embed_rows][H] fp32, or NULL
+  int n_embed_rows;
+  const int32_t *pos3;              // [3][n_pos] position streams, or NULL
+  int n_pos, pos0;
+  float *hidden;                    // [n][L+1][H] or NULL
+  int *err;                         // first error code (device)
+  float *x, *qkv, *attn, *y, *gate, *up;  // chunk scratch (fp32)
+  uint16_t *hh, *hm, *hl;           // GEMM input as bf16 hi + mid + lo
+};
+
+// per-layer weights (borrowed device pointers, bf16)
+struct PfLayer {
+  const uint16_t *attn_norm, *wq, *wk, *wv, *q_norm, *k_norm, *wo, *mlp_norm, *w_gate, *w_up, *w_down;
+};
+
+// scratch and the GEMM library handle, owned by an mk_handle
+struct PfState {
+  int tc = 0;                       // tokens per chunk the scratch holds
+  void *blas = nullptr;             // cublasHandle_t
+  float *x = nullptr, *qkv = nullptr, *attn = nullptr, *y = nullptr, *gate = nullptr, *up = nullptr;
+  float *logits = nullptr;          // [tc][V], allocated on first need
+  uint16_t *hh = nullptr, *hm = nullptr, *hl = nullptr;
+  int *err = nullptr;
+};
+
+int pf_init(PfState &st, int tc, int H, int Hq, int Hkv, int d, int I);
+void pf_free(PfState &st);
+
+// Run n prompt forwards (positions a.pos0 ..): fills the KV cache, writes
+// hidden / logits / out_ids when given, and the last token's greedy id to
+// *last_id (device).  Returns MK_OK or an MK_ERR_* code (after the stream
+// has completed).
+int pf_run(PfState &st, PfArgs a, const PfLayer *layers, const uint16_t *final_norm, const uint16_t *lm_head,
+           int n, int32_t *out_ids, float *logits_out, int *last_id, cudaStream_t s);
+
+}  // namespace mkp

@@ -57,6 +57,13 @@ def test_qwen3_0p6b_prompt32_greedy512():
     free = dec.decode(prompt, 512).cpu().numpy()
     k = first_near_tie(lg_ref)
     assert np.array_equal(free[:k], ids_ref[:k]), "greedy ids diverge before the first near tie (%d)" % k
+    # the batched prefill of the same 32-token prompt (tensor-core GEMMs)
+    dec.reset()
+    lgp = torch.full((32, s["vocab"]), float("nan"), dtype=torch.float32, device="cuda:0")
+    hdp = torch.full((32, s["n_layers"] + 1, s["hidden"]), float("nan"), dtype=torch.float32, device="cuda:0")
+    idp = dec.prefill(prompt, logits=lgp, hidden=hdp).cpu().numpy()
+    _compare("qwen3_0p6b prefill", s, idp, lgp.double().cpu().numpy(), hdp.double().cpu().numpy(),
+             ids_ref[:32], lg_ref[:32], hd_ref[:32])
     dec.close()
 
 
@@ -114,6 +121,7 @@ def test_long_context_4096_prompt_then_greedy():
     ref.V[:, :, :T] = Vp
     ref.pos = T
     ref.last_id = O.argmax_lowest(pl[0])
+    ref_last = ref.last_id
     del Kp, Vp
     ids_ref, lg_ref, hd_ref = ref.generate([], n_steps)
     # GPU: the prompt in one launch, then the greedy forwards teacher-forced
@@ -137,3 +145,15 @@ def test_long_context_4096_prompt_then_greedy():
     torch.cuda.synchronize()
     lg1 = lg1.double().cpu().numpy()
     assert np.abs(lg1 - lg).max() <= 1e-3 * max(1.0, np.abs(lg).max())
+    one.close()
+    # the 4096-token prompt through the batched prefill (16 chunks of 256),
+    # then the same teacher-forced greedy forwards
+    pf = mk.Decoder(s, w, max_seq=T + n_steps)
+    last = int(pf.prefill(prompt).cpu().numpy()[-1])
+    if pl[0][top[1]] - pl[0][top[0]] > 1e-2:
+        assert last == ref_last
+    else:
+        assert last in top
+    ids_p, lg_p, hd_p = _gpu_teacher_forced(pf, feed)
+    _compare("long_ctx after prefill", s, ids_p, lg_p, hd_p, ids_ref, lg_ref, hd_ref)
+    pf.close()

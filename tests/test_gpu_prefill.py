@@ -1,0 +1,108 @@
+"""Batched prompt prefill (``mk_prefill``): the prompt's forwards as batched
+tensor-core GEMMs plus the library's own attention / norm kernels, checked
+against the oracle's all-positions path (``prefix_forward``) and against the
+oracle's step path for the decode that continues after it."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+from parity_util import assert_close, assert_ids
+
+pytestmark = pytest.mark.gpu
+
+mk = pytest.importorskip("persistent_transformer_megakernel_gb300")
+
+
+def _prefill_then_decode(name, T, n_steps, max_seq, pos3_mode=None, sentinel=False):
+    s = W.shape(name)
+    w = W.make_weights(s, seed=0)
+    n = T + n_steps
+    pos3 = None if pos3_mode is None else W.make_pos3(0, n, distinct=(pos3_mode == "distinct"))
+    shp = O.DecoderShape.from_dict(s)
+    Wt = O.decoder.Weights(shp, w)
+    if sentinel:
+        rng = np.random.default_rng(11)
+        E = rng.standard_normal((T, s["hidden"])) * 0.02
+        prompt = W.sentinel_ids(T)
+    else:
+        E = None
+        prompt = W.make_prompt(s["vocab_in"], T, seed=1)
+    pl, ph, Kp, Vp = O.prefix_forward(shp, None, prompt, sentinel_rows=E,
+                                      pos3=None if pos3 is None else pos3[:, :T], weights=Wt)
+    ids_pre = np.array([O.argmax_lowest(r) for r in pl])
+    # the oracle's step path continues from the prefix state
+    ref = O.Decoder(shp, None, max_seq=max_seq, weights=Wt)
+    ref.K[:, :, :T] = Kp
+    ref.V[:, :, :T] = Vp
+    ref.pos = T
+    ref.last_id = int(ids_pre[-1])
+    ids_ref, lg_ref, hd_ref = ref.generate([], n_steps, pos3=None if pos3 is None else pos3[:, T:])
+    # GPU: prefill, then teacher-forced decode of the oracle's greedy ids
+    dec = mk.Decoder(s, w, max_seq=max_seq)
+    lg = torch.full((T, s["vocab"]), float("nan"), device="cuda:0")
+    hd = torch.full((T, s["n_layers"] + 1, s["hidden"]), float("nan"), device="cuda:0")
+    d_E = None if E is None else torch.as_tensor(E, dtype=torch.float32, device="cuda:0").contiguous()
+    p3 = None if pos3 is None else torch.as_tensor(pos3[:, :T].copy(), device="cuda:0").contiguous()
+    ids = dec.prefill(prompt, embeds=d_E, pos3=p3, logits=lg, hidden=hd).cpu().numpy()
+    torch.cuda.synchronize()
+    assert_close(lg.double().cpu().numpy(), pl, name + " prefill logits")
+    hdn = hd.double().cpu().numpy()
+    for l in range(s["n_layers"] + 1):
+        assert_close(hdn[:, l], ph[:, l], "%s prefill hidden[%d]" % (name, l))
+    assert_ids(ids, ids_pre, pl, name + " prefill ids")
+    if n_steps:
+        feed = np.concatenate([[ids_pre[-1]], ids_ref[:n_steps - 1]]).astype(np.int32)
+        lg2 = torch.full((n_steps, s["vocab"]), float("nan"), device="cuda:0")
+        p3d = None if pos3 is None else torch.as_tensor(pos3[:, T:].copy(), device="cuda:0").contiguous()
+        ids2 = dec.decode(feed, 0, logits=lg2, pos3=p3d).cpu().numpy()
+        torch.cuda.synchronize()
+        assert_close(lg2.double().cpu().numpy(), lg_ref, name + " decode after prefill")
+        assert_ids(ids2, ids_ref, lg_ref, name + " decode ids")
+    dec.close()
+
+
+@pytest.mark.parametrize("name,T,n_steps,max_seq", [
+    ("tiny", 8, 8, 32),
+    ("mid", 40, 12, 64),        # 0.6B-wide layers
+    ("gqa4", 20, 8, 40),        # group 4, head_dim 64, tied head
+    ("tiny", 300, 4, 320),      # two chunks of the 256-token scratch
+])
+def test_prefill_parity(name, T, n_steps, max_seq):
+    _prefill_then_decode(name, T, n_steps, max_seq)
+
+
+@pytest.mark.parametrize("name", ["mrope_small", "mrope_small_interleaved"])
+def test_prefill_mrope_distinct_streams(name):
+    _prefill_then_decode(name, 10, 6, 24, pos3_mode="distinct")
+
+
+def test_prefill_sentinel_rows():
+    _prefill_then_decode("mid", 12, 4, 24, sentinel=True)
+
+
+def test_prefill_last_id_only_and_errors():
+    # without ids only the last token's logits are computed; decode continues
+    # from its greedy id exactly as after a one-token-per-forward prompt
+    s = W.shape("mid")
+    w = W.make_weights(s, seed=0)
+    prompt = W.make_prompt(s["vocab_in"], 16, seed=1)
+    a = mk.Decoder(s, w, max_seq=40)
+    full = a.prefill(prompt).cpu().numpy()
+    a_next = a.decode(None, 6).cpu().numpy()
+    b = mk.Decoder(s, w, max_seq=40)
+    assert b.prefill(prompt, all_ids=False) is None
+    b_next = b.decode(None, 6).cpu().numpy()
+    assert np.array_equal(a_next, b_next)
+    assert b.info()["position"] == 22
+    # a bad id is reported, not faulted; the KV-full check is on the host
+    c = mk.Decoder(s, w, max_seq=40)
+    bad = prompt.copy()
+    bad[3] = s["vocab_in"]
+    with pytest.raises(mk.MKError):
+        c.prefill(bad)
+    d = mk.Decoder(s, w, max_seq=10)
+    with pytest.raises(mk.MKError):
+        d.prefill(prompt)
+    del full
