@@ -42,6 +42,11 @@ __device__ __forceinline__ void split3(float v, uint16_t &hi, uint16_t &mid, uin
   lo = f2bf(r1 - bf2f(mid));
 }
 
+// a GEMM output element: the sum of its three partials (one per input term)
+__device__ __forceinline__ float sum3(const float *c, size_t stride, size_t i) {
+  return (c[i] + c[stride + i]) + c[2 * stride + i];
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -85,6 +90,7 @@ __global__ void pf_embed(const PfArgs a, int t0, int nt) {
 // h = x / sqrt(mean(x^2) + eps) * gain as three bf16 terms
 __global__ void pf_add_norm_split(const PfArgs a, const float *y, const uint16_t *gain, int t0, int nt,
                                   int hidden_layer) {
+  // y: three partials of the GEMM output, a.y_stride apart, or NULL
   __shared__ float red[PF_THREADS / 32];
   const int t = blockIdx.x;
   if (t >= nt) return;
@@ -93,7 +99,7 @@ __global__ void pf_add_norm_split(const PfArgs a, const float *y, const uint16_t
   for (int k = threadIdx.x; k < a.H; k += blockDim.x) {
     float v = x[k];
     if (y) {
-      v = v + y[static_cast<size_t>(t) * a.H + k];
+      v = v + sum3(y, a.y_stride, static_cast<size_t>(t) * a.H + k);
       x[k] = v;
       if (a.hidden && hidden_layer >= 0)
         a.hidden[(static_cast<size_t>(t0 + t) * (a.L + 1) + hidden_layer) * a.H + k] = v;
@@ -105,26 +111,26 @@ __global__ void pf_add_norm_split(const PfArgs a, const float *y, const uint16_t
   const size_t o = static_cast<size_t>(t) * a.H;
   for (int k = threadIdx.x; k < a.H; k += blockDim.x) {
     const float h = x[k] * rs * bf2f(gain[k]);
-    split3(h, a.hh[o + k], a.hm[o + k], a.hl[o + k]);
+    split3(h, a.hs[o + k], a.hs[a.hs_stride + o + k], a.hs[2 * a.hs_stride + o + k]);
   }
 }
 
 // v (fp32, n per token) as three bf16 terms (the attention output before O)
-__global__ void pf_split(const float *v, int n, int nt, uint16_t *hi, uint16_t *mid, uint16_t *lo) {
+__global__ void pf_split(const float *v, int n, int nt, uint16_t *hs, size_t hs_stride) {
   const size_t total = static_cast<size_t>(n) * nt;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<size_t>(gridDim.x) * blockDim.x)
-    split3(v[i], hi[i], mid[i], lo[i]);
+    split3(v[i], hs[i], hs[hs_stride + i], hs[2 * hs_stride + i]);
 }
 
-// u = silu(gate) * up, as three bf16 terms
-__global__ void pf_silu_mul_split(const float *g, const float *u, int n, int nt, uint16_t *hi, uint16_t *mid,
-                                  uint16_t *lo) {
+// u = silu(gate) * up from the GEMM partials (c_stride apart), as three bf16 terms
+__global__ void pf_silu_mul_split(const float *g, const float *u, size_t c_stride, int n, int nt, uint16_t *hs,
+                                  size_t hs_stride) {
   const size_t total = static_cast<size_t>(n) * nt;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const float z = g[i];
-    split3(z / (1.0f + expf(-z)) * u[i], hi[i], mid[i], lo[i]);
+    const float z = sum3(g, c_stride, i);
+    split3(z / (1.0f + expf(-z)) * sum3(u, c_stride, i), hs[i], hs[hs_stride + i], hs[2 * hs_stride + i]);
   }
 }
 
@@ -153,10 +159,10 @@ __global__ void pf_qk_rope_append(const PfArgs a, int layer, const uint16_t *q_n
   const int t = warp / jobs, job = warp % jobs;
   const int P = a.pos0 + t0 + t;
   const int rows = (a.Hq + 2 * a.Hkv) * HD;
-  float *src = a.qkv + static_cast<size_t>(t) * rows + static_cast<size_t>(job) * HD;
+  const size_t base = static_cast<size_t>(t) * rows + static_cast<size_t>(job) * HD;
   float v[EPL];
 #pragma unroll
-  for (int k = 0; k < EPL; ++k) v[k] = src[lane + 32 * k];
+  for (int k = 0; k < EPL; ++k) v[k] = sum3(a.qkv3, a.qkv_stride, base + lane + 32 * k);
   if (job < a.Hq + a.Hkv) {
     const uint16_t *gain = job < a.Hq ? q_norm : k_norm;
     float ss = 0.f;
@@ -183,7 +189,7 @@ __global__ void pf_qk_rope_append(const PfArgs a, int layer, const uint16_t *q_n
   }
   if (job < a.Hq) {
 #pragma unroll
-    for (int k = 0; k < EPL; ++k) src[lane + 32 * k] = v[k] * a.inv_sqrt_d;
+    for (int k = 0; k < EPL; ++k) a.qkv[base + lane + 32 * k] = v[k] * a.inv_sqrt_d;
   } else {
     const bool key = job < a.Hq + a.Hkv;
     const int g = key ? job - a.Hq : job - a.Hq - a.Hkv;
@@ -245,34 +251,64 @@ __global__ void pf_attention(const PfArgs a, int layer, int t0, int nt) {
   }
 }
 
-// greedy id of each token: the largest logit, the lowest index among equals;
-// a non-finite logit is an error
-__global__ void pf_argmax(const float *logits, int V, int nt, int t_first, int32_t *out_ids, int *last_id,
-                          int t_last, int *err) {
-  __shared__ float bv[PF_THREADS / 32];
-  __shared__ int bi[PF_THREADS / 32];
-  const int t = blockIdx.x;
-  if (t >= nt) return;
-  const float *row = logits + static_cast<size_t>(t) * V;
+// Greedy id of each token, in two stages: block (t, b) sums the three logit
+// partials of its slice of the vocabulary (storing them in logits_out when
+// given) and keeps its best (largest value, lowest index among equals); then
+// one warp per token reduces the blocks' candidates.  A non-finite logit is
+// an error.
+constexpr int PF_ARGMAX_BLOCKS = 64;
+
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
+
+__global__ void pf_argmax_part(const float *lg3, size_t stride, int V, int t_first, float *logits_out, float *pv,
+                               int *pi, int *err) {
+  __shared__ float sv[PF_THREADS / 32];
+  __shared__ int si[PF_THREADS / 32];
+  const int t = blockIdx.y, b = blockIdx.x;
+  const int per = (V + PF_ARGMAX_BLOCKS - 1) / PF_ARGMAX_BLOCKS;
+  const int k0 = b * per, k1 = min(V, k0 + per);
   float v = -INFINITY;
   int i = 0x7fffffff;
-  for (int k = threadIdx.x; k < V; k += blockDim.x) {
-    const float y = row[k];
+  for (int k = k0 + threadIdx.x; k < k1; k += blockDim.x) {
+    const float y = sum3(lg3, stride, static_cast<size_t>(t) * V + k);
+    if (logits_out) logits_out[static_cast<size_t>(t_first + t) * V + k] = y;
     if (!isfinite(y)) atomicCAS(err, 0, MK_PF_ERR_NUMERIC);
-    if (y > v || (y == v && k < i)) { v = y; i = k; }
+    if (better(y, k, v, i)) { v = y; i = k; }
   }
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
     const float ov = __shfl_xor_sync(0xffffffffu, v, o);
     const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-    if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
+    if (better(ov, oi, v, i)) { v = ov; i = oi; }
   }
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) { bv[w] = v; bi[w] = i; }
+  if (lane == 0) { sv[w] = v; si[w] = i; }
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int k = 1; k < PF_THREADS / 32; ++k)
-      if (bv[k] > v || (bv[k] == v && bi[k] < i)) { v = bv[k]; i = bi[k]; }
+      if (better(sv[k], si[k], v, i)) { v = sv[k]; i = si[k]; }
+    pv[t * PF_ARGMAX_BLOCKS + b] = v;
+    pi[t * PF_ARGMAX_BLOCKS + b] = i;
+  }
+}
+
+__global__ void pf_argmax_final(const float *pv, const int *pi, int t_first, int32_t *out_ids, int *last_id,
+                                int t_last) {
+  const int t = blockIdx.x, lane = threadIdx.x;
+  float v = -INFINITY;
+  int i = 0x7fffffff;
+  for (int b = lane; b < PF_ARGMAX_BLOCKS; b += 32)
+    if (better(pv[t * PF_ARGMAX_BLOCKS + b], pi[t * PF_ARGMAX_BLOCKS + b], v, i)) {
+      v = pv[t * PF_ARGMAX_BLOCKS + b];
+      i = pi[t * PF_ARGMAX_BLOCKS + b];
+    }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (better(ov, oi, v, i)) { v = ov; i = oi; }
+  }
+  if (lane == 0) {
     if (out_ids) out_ids[t_first + t] = i;
     if (last_id && t_first + t == t_last) *last_id = i;
   }
@@ -296,16 +332,16 @@ int dalloc(T **p, size_t n) {
   return MK_OK;
 }
 
-// C[nt][N] (ldc) = (hi + mid + lo)[nt][K] . W[N][K]^T, fp32 accumulate on tensor
-// cores: in column-major terms C^T (N x nt) = W (N x K, stored as K x N) . in^T
-int gemm3(cublasHandle_t b, const uint16_t *hi, const uint16_t *mid, const uint16_t *lo, const uint16_t *W, int nt,
-          int N, int K, float *C, int ldc) {
+// C_i[nt][N] (ldc) = term_i[nt][K] . W[N][K]^T for the three bf16 terms of the
+// input (term i at in + i * in_stride, C_i at C + i * c_stride), fp32 accumulate
+// on tensor cores, one batched call; the readers add C_0 + C_1 + C_2.  In
+// column-major terms C_i^T (N x nt) = W (N x K, stored as K x N) . term_i^T.
+int gemm3(cublasHandle_t b, const uint16_t *in, long long in_stride, const uint16_t *W, int nt, int N, int K,
+          float *C, int ldc, long long c_stride) {
   const float one = 1.0f, zero = 0.0f;
-  const uint16_t *terms[3] = {hi, mid, lo};
-  cublasStatus_t st = CUBLAS_STATUS_SUCCESS;
-  for (int i = 0; i < 3 && st == CUBLAS_STATUS_SUCCESS; ++i)
-    st = cublasGemmEx(b, CUBLAS_OP_T, CUBLAS_OP_N, N, nt, K, &one, W, CUDA_R_16BF, K, terms[i], CUDA_R_16BF, K,
-                      i == 0 ? &zero : &one, C, CUDA_R_32F, ldc, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+  const cublasStatus_t st = cublasGemmStridedBatchedEx(
+      b, CUBLAS_OP_T, CUBLAS_OP_N, N, nt, K, &one, W, CUDA_R_16BF, K, 0, in, CUDA_R_16BF, K, in_stride, &zero, C,
+      CUDA_R_32F, ldc, c_stride, 3, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
   return st == CUBLAS_STATUS_SUCCESS ? MK_OK : MK_ERR_CUDA;
 }
 
@@ -323,22 +359,23 @@ int pf_init(PfState &st, int tc, int H, int Hq, int Hkv, int d, int I) {
   cublasHandle_t b = nullptr;
   if (cublasCreate(&b) != CUBLAS_STATUS_SUCCESS) return MK_ERR_CUDA;
   st.blas = b;
+  const size_t T = tc;
   int rc;
-  if ((rc = dalloc(&st.x, static_cast<size_t>(tc) * H)) || (rc = dalloc(&st.qkv, static_cast<size_t>(tc) * rows)) ||
-      (rc = dalloc(&st.attn, static_cast<size_t>(tc) * Hq * d)) || (rc = dalloc(&st.y, static_cast<size_t>(tc) * H)) ||
-      (rc = dalloc(&st.gate, static_cast<size_t>(tc) * I)) || (rc = dalloc(&st.up, static_cast<size_t>(tc) * I)) ||
-      (rc = dalloc(&st.hh, static_cast<size_t>(tc) * kmax)) || (rc = dalloc(&st.hm, static_cast<size_t>(tc) * kmax)) ||
-      (rc = dalloc(&st.hl, static_cast<size_t>(tc) * kmax)) ||
-      (rc = dalloc(&st.err, 1))) {
+  if ((rc = dalloc(&st.x, T * H)) || (rc = dalloc(&st.qkv, T * rows)) || (rc = dalloc(&st.attn, T * Hq * d)) ||
+      (rc = dalloc(&st.qkv3, 3 * T * rows)) || (rc = dalloc(&st.y3, 3 * T * H)) ||
+      (rc = dalloc(&st.gate3, 3 * T * I)) || (rc = dalloc(&st.up3, 3 * T * I)) ||
+      (rc = dalloc(&st.hs, 3 * T * kmax)) || (rc = dalloc(&st.pv, T * PF_ARGMAX_BLOCKS)) ||
+      (rc = dalloc(&st.pi, T * PF_ARGMAX_BLOCKS)) || (rc = dalloc(&st.err, 1))) {
     pf_free(st);
     return rc;
   }
   st.tc = tc;
+  st.kmax = kmax;
   return MK_OK;
 }
 
 void pf_free(PfState &st) {
-  void *ps[] = {st.x, st.qkv, st.attn, st.y, st.gate, st.up, st.logits, st.hh, st.hm, st.hl, st.err};
+  void *ps[] = {st.x, st.qkv, st.attn, st.qkv3, st.y3, st.gate3, st.up3, st.logits3, st.pv, st.pi, st.hs, st.err};
   for (void *p : ps)
     if (p) cudaFree(p);
   if (st.blas) cublasDestroy(static_cast<cublasHandle_t>(st.blas));
@@ -349,18 +386,24 @@ int pf_run(PfState &st, PfArgs a, const PfLayer *layers, const uint16_t *final_n
            int n, int32_t *out_ids, float *logits_out, int *last_id, cudaStream_t s) {
   cublasHandle_t b = static_cast<cublasHandle_t>(st.blas);
   if (cublasSetStream(b, s) != CUBLAS_STATUS_SUCCESS) return MK_ERR_CUDA;
-  const bool all_logits = out_ids || logits_out;
-  if (all_logits && !logits_out && !st.logits) {
-    int rc = dalloc(&st.logits, static_cast<size_t>(st.tc) * a.V);
-    if (rc) return rc;
-  }
-  a.x = st.x; a.qkv = st.qkv; a.attn = st.attn; a.y = st.y; a.gate = st.gate; a.up = st.up;
-  a.hh = st.hh; a.hm = st.hm; a.hl = st.hl; a.err = st.err;
-  if (cudaMemsetAsync(st.err, 0, sizeof(int), s) != cudaSuccess) return MK_ERR_CUDA;
   const int rows = (a.Hq + 2 * a.Hkv) * a.d;
   const int grp = a.Hq / a.Hkv;
   if ((a.d != 64 && a.d != 128) || a.Hq % a.Hkv || (grp != 1 && grp != 2 && grp != 4 && !(grp == 8 && a.d == 64)))
     return MK_ERR_UNSUPPORTED;
+  const size_t T = st.tc;
+  if (!st.logits3) {
+    int rc = dalloc(&st.logits3, 3 * T * a.V);
+    if (rc) return rc;
+  }
+  a.x = st.x; a.qkv = st.qkv; a.attn = st.attn;
+  a.qkv3 = st.qkv3; a.qkv_stride = T * rows;
+  a.y3 = st.y3; a.y_stride = T * a.H;
+  a.hs = st.hs; a.hs_stride = T * st.kmax;
+  a.err = st.err;
+  const long long hs_s = static_cast<long long>(a.hs_stride);
+  const long long ffn_s = static_cast<long long>(T) * a.I, lg_s = static_cast<long long>(T) * a.V;
+  if (cudaMemsetAsync(st.err, 0, sizeof(int), s) != cudaSuccess) return MK_ERR_CUDA;
+  const bool all_logits = out_ids || logits_out;
   int rc = MK_OK;
   for (int t0 = 0; t0 < n && rc == MK_OK; t0 += st.tc) {
     const int nt = n - t0 < st.tc ? n - t0 : st.tc;
@@ -369,9 +412,10 @@ int pf_run(PfState &st, PfArgs a, const PfLayer *layers, const uint16_t *final_n
     for (int l = 0; l < a.L && rc == MK_OK; ++l) {
       const PfLayer &w = layers[l];
       // attention block
-      if ((rc = gemm3(b, st.hh, st.hm, st.hl, w.wq, nt, a.Hq * a.d, a.H, st.qkv, rows)) ||
-          (rc = gemm3(b, st.hh, st.hm, st.hl, w.wk, nt, a.Hkv * a.d, a.H, st.qkv + a.Hq * a.d, rows)) ||
-          (rc = gemm3(b, st.hh, st.hm, st.hl, w.wv, nt, a.Hkv * a.d, a.H, st.qkv + (a.Hq + a.Hkv) * a.d, rows)))
+      if ((rc = gemm3(b, st.hs, hs_s, w.wq, nt, a.Hq * a.d, a.H, st.qkv3, rows, a.qkv_stride)) ||
+          (rc = gemm3(b, st.hs, hs_s, w.wk, nt, a.Hkv * a.d, a.H, st.qkv3 + a.Hq * a.d, rows, a.qkv_stride)) ||
+          (rc = gemm3(b, st.hs, hs_s, w.wv, nt, a.Hkv * a.d, a.H, st.qkv3 + (a.Hq + a.Hkv) * a.d, rows,
+                      a.qkv_stride)))
         break;
       const int jobs_warps = nt * (a.Hq + 2 * a.Hkv), attn_warps = nt * a.Hkv;
       const int wpb = PF_THREADS / 32;
@@ -392,35 +436,30 @@ int pf_run(PfState &st, PfArgs a, const PfLayer *layers, const uint16_t *final_n
         }
       }
       pf_split<<<blocks_for(static_cast<size_t>(nt) * a.Hq * a.d), PF_THREADS, 0, s>>>(st.attn, a.Hq * a.d, nt,
-                                                                                         st.hh, st.hm, st.hl);
-      if ((rc = gemm3(b, st.hh, st.hm, st.hl, w.wo, nt, a.H, a.Hq * a.d, st.y, a.H))) break;
-      pf_add_norm_split<<<nt, PF_THREADS, 0, s>>>(a, st.y, w.mlp_norm, t0, nt, -1);
+                                                                                         st.hs, a.hs_stride);
+      if ((rc = gemm3(b, st.hs, hs_s, w.wo, nt, a.H, a.Hq * a.d, st.y3, a.H, a.y_stride))) break;
+      pf_add_norm_split<<<nt, PF_THREADS, 0, s>>>(a, st.y3, w.mlp_norm, t0, nt, -1);
       // MLP block
-      if ((rc = gemm3(b, st.hh, st.hm, st.hl, w.w_gate, nt, a.I, a.H, st.gate, a.I)) ||
-          (rc = gemm3(b, st.hh, st.hm, st.hl, w.w_up, nt, a.I, a.H, st.up, a.I)))
+      if ((rc = gemm3(b, st.hs, hs_s, w.w_gate, nt, a.I, a.H, st.gate3, a.I, ffn_s)) ||
+          (rc = gemm3(b, st.hs, hs_s, w.w_up, nt, a.I, a.H, st.up3, a.I, ffn_s)))
         break;
-      pf_silu_mul_split<<<blocks_for(static_cast<size_t>(nt) * a.I), PF_THREADS, 0, s>>>(st.gate, st.up, a.I, nt,
-                                                                                         st.hh, st.hm, st.hl);
-      if ((rc = gemm3(b, st.hh, st.hm, st.hl, w.w_down, nt, a.H, a.I, st.y, a.H))) break;
-      pf_add_norm_split<<<nt, PF_THREADS, 0, s>>>(a, st.y, l + 1 < a.L ? layers[l + 1].attn_norm : final_norm, t0,
+      pf_silu_mul_split<<<blocks_for(static_cast<size_t>(nt) * a.I), PF_THREADS, 0, s>>>(
+          st.gate3, st.up3, static_cast<size_t>(ffn_s), a.I, nt, st.hs, a.hs_stride);
+      if ((rc = gemm3(b, st.hs, hs_s, w.w_down, nt, a.H, a.I, st.y3, a.H, a.y_stride))) break;
+      pf_add_norm_split<<<nt, PF_THREADS, 0, s>>>(a, st.y3, l + 1 < a.L ? layers[l + 1].attn_norm : final_norm, t0,
                                                    nt, l + 1);
     }
     if (rc != MK_OK) break;
     // LM head: every token of the chunk when ids or logits are wanted, else
     // only the prompt's last token (the first generated id)
     const bool has_last = (t0 + nt == n);
-    if (all_logits) {
-      float *lg = logits_out ? logits_out + static_cast<size_t>(t0) * a.V : st.logits;
-      if ((rc = gemm3(b, st.hh, st.hm, st.hl, lm_head, nt, a.V, a.H, lg, a.V))) break;
-      pf_argmax<<<nt, PF_THREADS, 0, s>>>(lg, a.V, nt, t0, out_ids, last_id, n - 1, st.err);
-    } else if (has_last) {
-      if (!st.logits) {
-        // one row suffices here
-        if ((rc = dalloc(&st.logits, static_cast<size_t>(st.tc) * a.V))) break;
-      }
-      const size_t off = static_cast<size_t>(nt - 1) * a.H;
-      if ((rc = gemm3(b, st.hh + off, st.hm + off, st.hl + off, lm_head, 1, a.V, a.H, st.logits, a.V))) break;
-      pf_argmax<<<1, PF_THREADS, 0, s>>>(st.logits, a.V, 1, n - 1, nullptr, last_id, n - 1, st.err);
+    if (all_logits || has_last) {
+      const int first = all_logits ? 0 : nt - 1, m = all_logits ? nt : 1;
+      const size_t off = static_cast<size_t>(first) * a.H;
+      if ((rc = gemm3(b, st.hs + off, hs_s, lm_head, m, a.V, a.H, st.logits3, a.V, lg_s))) break;
+      pf_argmax_part<<<dim3(PF_ARGMAX_BLOCKS, m), PF_THREADS, 0, s>>>(st.logits3, static_cast<size_t>(lg_s), a.V,
+                                                                     t0 + first, logits_out, st.pv, st.pi, st.err);
+      pf_argmax_final<<<m, 32, 0, s>>>(st.pv, st.pi, t0 + first, out_ids, last_id, n - 1);
     }
   }
   if (cudaGetLastError() != cudaSuccess && rc == MK_OK) rc = MK_ERR_CUDA;

@@ -28,8 +28,11 @@ struct PfArgs {
   int n_pos, pos0;
   float *hidden;                    // [n][L+1][H] or NULL
   int *err;                         // first error code (device)
-  float *x, *qkv, *attn, *y, *gate, *up;  // chunk scratch (fp32)
-  uint16_t *hh, *hm, *hl;           // GEMM input as bf16 hi + mid + lo
+  float *x, *qkv, *attn;            // chunk scratch (fp32): residual, normed q, attention output
+  float *qkv3, *y3;                 // GEMM outputs as three partials, qkv_stride / y_stride apart
+  size_t qkv_stride, y_stride;
+  uint16_t *hs;                     // GEMM input as three bf16 terms (hi, mid, lo), hs_stride apart
+  size_t hs_stride;
 };
 
 // per-layer weights (borrowed device pointers, bf16)
@@ -41,9 +44,13 @@ struct PfLayer {
 struct PfState {
   int tc = 0;                       // tokens per chunk the scratch holds
   void *blas = nullptr;             // cublasHandle_t
-  float *x = nullptr, *qkv = nullptr, *attn = nullptr, *y = nullptr, *gate = nullptr, *up = nullptr;
-  float *logits = nullptr;          // [tc][V], allocated on first need
-  uint16_t *hh = nullptr, *hm = nullptr, *hl = nullptr;
+  float *x = nullptr, *qkv = nullptr, *attn = nullptr;
+  float *qkv3 = nullptr, *y3 = nullptr, *gate3 = nullptr, *up3 = nullptr;  // [3][tc][N] GEMM partials
+  float *logits3 = nullptr;         // [3][tc][V], allocated on the first LM head
+  float *pv = nullptr;              // argmax candidates [tc][blocks]
+  int *pi = nullptr;
+  uint16_t *hs = nullptr;           // [3][tc][kmax] bf16 input terms
+  size_t kmax = 0;
   int *err = nullptr;
 };
 
