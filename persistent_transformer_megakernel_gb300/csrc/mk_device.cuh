@@ -815,21 +815,33 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
       m[h] = -INFINITY;
       ls[h] = 0.f;
     }
-    auto visit = [&](const float (&kk)[EPL], const float (&vv)[EPL]) {
+    // score of one cached position for every head of the group (warp-reduced)
+    auto score = [&](const float (&kk)[EPL], float (&sv)[GRP]) {
 #pragma unroll
       for (int h = 0; h < GRP; ++h) {
-        float s = 0.f;
+        float x = 0.f;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) s = fmaf(q[h][e], kk[e], s);
-        s = warp_sum(s);
-        const float mn = fmaxf(m[h], s);
+        for (int e = 0; e < EPL; ++e) x = fmaf(q[h][e], kk[e], x);
+        sv[h] = warp_sum(x);
+      }
+    };
+    // online-softmax update with one position's scores and value row
+    auto update = [&](const float (&sv)[GRP], const float (&vv)[EPL]) {
+#pragma unroll
+      for (int h = 0; h < GRP; ++h) {
+        const float mn = fmaxf(m[h], sv[h]);
         const float sc = expf(m[h] - mn);
-        const float pe = expf(s - mn);
+        const float pe = expf(sv[h] - mn);
         ls[h] = ls[h] * sc + pe;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) o[h][e] = fmaf(pe, vv[e], o[h][e] * sc);
         m[h] = mn;
       }
+    };
+    auto visit = [&](const float (&kk)[EPL], const float (&vv)[EPL]) {
+      float sv[GRP];
+      score(kk, sv);
+      update(sv, vv);
     };
     for (int p0 = a; p0 < pend; p0 += TP) {
       const int np = min(TP, pend - p0);
@@ -837,12 +849,32 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
       const uint32_t par = (it / static_cast<uint32_t>(p.stages)) & 1u;
       wait_full(p, S, slot, par);
       const unsigned char *st = ring + static_cast<size_t>(slot) * p.stage_bytes;
-      for (int i = w; i < np; i += NCW) {
-        float kk[EPL], vv[EPL];
-        const uint16_t *kr = reinterpret_cast<const uint16_t *>(st) + static_cast<size_t>(i) * HD + lane * EPL;
-        const uint16_t *vr = reinterpret_cast<const uint16_t *>(st) + static_cast<size_t>(np + i) * HD + lane * EPL;
+      const uint16_t *kt = reinterpret_cast<const uint16_t *>(st) + lane * EPL;
+      const uint16_t *vt = kt + static_cast<size_t>(np) * HD;
+      int i = w;
+      // two positions at a time: their scores' warp reductions overlap; the
+      // updates still run in position order (the same arithmetic as one by one)
+      for (; i + NCW < np; i += 2 * NCW) {
+        float kk[2][EPL], vv[2][EPL], sv[2][GRP];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) { kk[e] = bf2f(kr[e]); vv[e] = bf2f(vr[e]); }
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) {
+            kk[j][e] = bf2f(kt[static_cast<size_t>(i + j * NCW) * HD + e]);
+            vv[j][e] = bf2f(vt[static_cast<size_t>(i + j * NCW) * HD + e]);
+          }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) score(kk[j], sv[j]);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) update(sv[j], vv[j]);
+      }
+      for (; i < np; i += NCW) {
+        float kk[EPL], vv[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          kk[e] = bf2f(kt[static_cast<size_t>(i) * HD + e]);
+          vv[e] = bf2f(vt[static_cast<size_t>(i) * HD + e]);
+        }
         visit(kk, vv);
       }
       __syncwarp();
