@@ -463,6 +463,28 @@ def ncu_case(args):
     print("ncu case done: %s, 16 prompt forwards then 8 greedy forwards" % args.workload)
 
 
+def prefill_case(args):
+    """The prefill launch list's case: the workload's prompt through
+    ``mk_prefill`` twice (only the last token's logits), device time printed."""
+    import torch
+    import persistent_transformer_megakernel_gb300 as mk
+    wl, s, _ = workload_desc(args.workload)
+    w = W.make_weights(s, seed=0)
+    n = wl["prompt"]
+    dec = mk.Decoder(s, w, max_seq=n + 8)
+    prompt = torch.as_tensor(W.make_prompt(s["vocab_in"], n, seed=1), device="cuda")
+    for rep in range(2):
+        dec.reset()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dec.prefill(prompt, all_ids=False)
+        e1.record()
+        e1.synchronize()
+        print("prefill case %d: %s, %d-token prompt, %.3f ms" % (rep, args.workload, n, e0.elapsed_time(e1)))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -474,9 +496,14 @@ def main():
     ap.add_argument("--ablation-forwards", type=int, default=32)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-ablation", action="store_true")
+    ap.add_argument("--prefill-case", action="store_true",
+                    help="run the workload's prompt through mk_prefill twice (the prefill ncu launch list)")
     ap.add_argument("--ncu-case", action="store_true",
                     help="run only the small profiling case (no JSON line)")
     args = ap.parse_args()
+    if args.prefill_case:
+        prefill_case(args)
+        return
     if args.ncu_case:
         ncu_case(args)
         return
