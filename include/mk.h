@@ -5,6 +5,10 @@
  * cooperatively launched kernel that loops over layers and decode steps
  * without exiting ("launch one kernel that owns the GPU and loops over decode
  * steps internally", page A section "The idea: one kernel that never exits").
+ * Around that loop: a batched prompt prefill on tensor cores (mk_prefill), a
+ * streaming mailbox the kernel fills with each greedy id while it runs
+ * (mk_decode_start / mk_mailbox_read), and the per-op ablation of the same
+ * math, plain or replayed from a CUDA graph (MK_DECODE_PER_OP*).
  *
  * Sources cited below:
  *   page A = "Porting a 1,200-line persistent CUDA megakernel to Qwen3-TTS:

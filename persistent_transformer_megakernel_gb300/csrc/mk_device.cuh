@@ -7,13 +7,18 @@
 // copies.  Weight streaming does not depend on the data, so the producer runs
 // ahead across grid barriers and decode steps while the consumers wait.
 //
-// Per forward (one token), the phases and their grid barriers are
+// Per forward (one token), the phases are
 //   per layer: QKV (RMSNorm fused) | attention (QK-norm, RoPE/MRoPE, KV append,
-//              split-KV partials, last-arriving CTA merges) | O-proj + residual
+//              split-KV chunk states; up to 8 chunks the chunk holding the new
+//              position polls the others and merges, more chunks: the
+//              last-arriving CTA merges) | O-proj + residual
 //              | RMSNorm + gate/up + SiLU*mul | down-proj + residual
-//   then:      final RMSNorm + LM head + per-CTA argmax candidates
+//   then:      final RMSNorm + LM head + per-CTA argmax candidates, and the
+//              forward's one grid barrier
 // and the next forward's first phase reduces the candidates (greedy argmax,
-// lowest index on ties) and feeds the id back in-kernel.
+// lowest index on ties) and feeds the id back in-kernel.  Between phases the
+// activations travel as tagged words (value + forward tag) that each reader
+// polls; there is no grid barrier inside a forward.
 //
 // page A = "Porting a 1,200-line persistent CUDA megakernel to Qwen3-TTS: ~25 ms
 // to first audio chunk" (dev.to); page B = "I made a single CUDA kernel speak:
