@@ -169,6 +169,19 @@ def cpu_oracle_rate(workload: str, n_forwards: int, threads: int, warmup: int = 
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
+def reduce_timing(total_ms, units_per_rank, world, device="cpu"):
+    """Whole-job throughput of `world` independent replicas: the slowest
+    rank's time (all-reduce MAX over the process group) against the units all
+    ranks processed.  Returns (max_ms, units per second)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms, units_per_rank * world / (total_ms / 1e3)
+
+
 def cpu_threads():
     try:
         return len(os.sched_getaffinity(0))
@@ -293,14 +306,9 @@ def run_gpu(args, rank, world):
         total_ms += e0.elapsed_time(e1)
     torch.cuda.synchronize()
     clocks = sampler.stop()
+    total_ms, value = reduce_timing(total_ms, n_timed * args.steps, world, dev)
     if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
         dist.barrier()
-
-    tokens = n_timed * args.steps * world
-    value = tokens / (total_ms / 1e3)
     per_launch_ms = total_ms / args.steps
     bytes_launch = algorithmic_bytes(s, info["weight_bytes"], timed_positions)
     peak, peak_src = load_peaks()
