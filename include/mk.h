@@ -217,10 +217,14 @@ int mk_decode(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_ste
  *   logits ([n][vocab]) and hidden ([n][L+1][H]) as for mk_decode; flags,
  *   trace and code rows must be unset.  Not bitwise equal to mk_decode (other
  *   summation orders); both follow the oracle within the parity tolerance.
+ * The first call of a handle creates its GEMM library handle and scratch for
+ * 256-token chunks (about 0.5 GB at the 0.6B shape); the launch sequence of
+ * each prompt length is captured as a CUDA graph on its first use and replayed
+ * afterwards (the call's ids, cursor and output pointers are read from device
+ * memory, so a replay serves any call of that length).
  * Blocks until `stream` completes.  Errors: MK_ERR_INVALID_ARG, MK_ERR_KV_FULL,
- * MK_ERR_BAD_TOKEN, MK_ERR_BAD_POSITION, MK_ERR_NUMERIC, MK_ERR_NO_MEMORY
- * (scratch for 256 tokens is allocated on the first call), MK_ERR_UNSUPPORTED,
- * MK_ERR_CUDA. */
+ * MK_ERR_BAD_TOKEN, MK_ERR_BAD_POSITION, MK_ERR_NUMERIC, MK_ERR_NO_MEMORY,
+ * MK_ERR_UNSUPPORTED, MK_ERR_CUDA. */
 int mk_prefill(mk_handle *h, const int32_t *d_in_ids, int32_t n, int32_t *d_out_ids,
                const mk_decode_opts *opts, mk_stream stream);
 

@@ -605,9 +605,12 @@ int mk_prefill(mk_handle *h, const int32_t *d_in_ids, int32_t n, int32_t *d_out_
   a.rope_mode = p.rope_mode; a.sec0 = p.sec_b0; a.sec1 = p.sec1; a.sec2 = p.sec2;
   a.rope_len = p.rope_len; a.max_seq = p.max_seq;
   a.embed = p.embed; a.rope = p.rope; a.kcache = p.kcache; a.vcache = p.vcache;
-  a.ids = d_in_ids; a.embeds = o.embeds; a.n_embed_rows = o.embeds ? o.n_embed_rows : 0;
-  a.pos3 = o.pos3; a.n_pos = n; a.pos0 = h->pos; a.hidden = o.hidden;
-  rc = mkp::pf_run(h->pf, a, h->pf_layers.data(), p.final_norm, p.lm_head, n, d_out_ids, o.logits, p.last_id,
+  mkp::PfCall call;
+  std::memset(&call, 0, sizeof(call));
+  call.ids = d_in_ids; call.embeds = o.embeds; call.n_embed_rows = o.embeds ? o.n_embed_rows : 0;
+  call.pos3 = o.pos3; call.n_pos = n; call.pos0 = h->pos; call.hidden = o.hidden;
+  call.out_ids = d_out_ids; call.logits_out = o.logits; call.last_id = p.last_id;
+  rc = mkp::pf_run(h->pf, a, h->pf_layers.data(), p.final_norm, p.lm_head, n, call,
                    reinterpret_cast<cudaStream_t>(stream));
   if (rc != MK_OK) return rc;
   h->pos += n;

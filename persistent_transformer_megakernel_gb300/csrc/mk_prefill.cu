@@ -71,8 +71,9 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
 __global__ void pf_embed(const PfArgs a, int t0, int nt) {
   const int t = blockIdx.x;
   if (t >= nt) return;
-  const int id = a.ids[t0 + t];
-  const bool bad = id >= 0 ? id >= a.vocab_in : (!a.embeds || -(id + 1) >= a.n_embed_rows);
+  const PfCall &c = *a.call;
+  const int id = c.ids[t0 + t];
+  const bool bad = id >= 0 ? id >= a.vocab_in : (!c.embeds || -(id + 1) >= c.n_embed_rows);
   if (bad) {
     if (threadIdx.x == 0) atomicCAS(a.err, 0, MK_PF_ERR_BAD_TOKEN);
     return;
@@ -80,9 +81,9 @@ __global__ void pf_embed(const PfArgs a, int t0, int nt) {
   float *x = a.x + static_cast<size_t>(t) * a.H;
   for (int k = threadIdx.x; k < a.H; k += blockDim.x) {
     const float v = id >= 0 ? bf2f(a.embed[static_cast<size_t>(id) * a.H + k])
-                            : a.embeds[static_cast<size_t>(-(id + 1)) * a.H + k];
+                            : c.embeds[static_cast<size_t>(-(id + 1)) * a.H + k];
     x[k] = v;
-    if (a.hidden) a.hidden[(static_cast<size_t>(t0 + t) * (a.L + 1)) * a.H + k] = v;
+    if (c.hidden) c.hidden[(static_cast<size_t>(t0 + t) * (a.L + 1)) * a.H + k] = v;
   }
 }
 
@@ -101,8 +102,8 @@ __global__ void pf_add_norm_split(const PfArgs a, const float *y, const uint16_t
     if (y) {
       v = v + sum3(y, a.y_stride, static_cast<size_t>(t) * a.H + k);
       x[k] = v;
-      if (a.hidden && hidden_layer >= 0)
-        a.hidden[(static_cast<size_t>(t0 + t) * (a.L + 1) + hidden_layer) * a.H + k] = v;
+      if (a.call->hidden && hidden_layer >= 0)
+        a.call->hidden[(static_cast<size_t>(t0 + t) * (a.L + 1) + hidden_layer) * a.H + k] = v;
     }
     ss = fmaf(v, v, ss);
   }
@@ -157,7 +158,8 @@ __global__ void pf_qk_rope_append(const PfArgs a, int layer, const uint16_t *q_n
   const int jobs = a.Hq + 2 * a.Hkv;
   if (warp >= nt * jobs) return;
   const int t = warp / jobs, job = warp % jobs;
-  const int P = a.pos0 + t0 + t;
+  const PfCall &c = *a.call;
+  const int P = c.pos0 + t0 + t;
   const int rows = (a.Hq + 2 * a.Hkv) * HD;
   const size_t base = static_cast<size_t>(t) * rows + static_cast<size_t>(job) * HD;
   float v[EPL];
@@ -176,7 +178,7 @@ __global__ void pf_qk_rope_append(const PfArgs a, int layer, const uint16_t *q_n
     for (int k = 0; k < EPL / 2; ++k) {
       const int i = lane + 32 * k;
       const int s = pf_pair_stream(a, i);
-      int pos = a.pos3 ? a.pos3[static_cast<size_t>(s) * a.n_pos + t0 + t] : P;
+      int pos = c.pos3 ? c.pos3[static_cast<size_t>(s) * c.n_pos + t0 + t] : P;
       if (pos < 0 || pos >= a.rope_len) {
         atomicCAS(a.err, 0, MK_PF_ERR_BAD_POSITION);
         pos = 0;
@@ -209,7 +211,7 @@ __global__ void pf_attention(const PfArgs a, int layer, int t0, int nt) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= nt * a.Hkv) return;
   const int t = warp / a.Hkv, g = warp % a.Hkv;
-  const int P = a.pos0 + t0 + t;
+  const int P = a.call->pos0 + t0 + t;
   const int rows = (a.Hq + 2 * a.Hkv) * HD;
   float q[GRP][EPL], o[GRP][EPL], m[GRP], l[GRP];
 #pragma unroll
@@ -260,8 +262,9 @@ constexpr int PF_ARGMAX_BLOCKS = 64;
 
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
-__global__ void pf_argmax_part(const float *lg3, size_t stride, int V, int t_first, float *logits_out, float *pv,
+__global__ void pf_argmax_part(const float *lg3, size_t stride, int V, int t_first, const PfCall *call, float *pv,
                                int *pi, int *err) {
+  float *logits_out = call->logits_out;
   __shared__ float sv[PF_THREADS / 32];
   __shared__ int si[PF_THREADS / 32];
   const int t = blockIdx.y, b = blockIdx.x;
@@ -292,9 +295,10 @@ __global__ void pf_argmax_part(const float *lg3, size_t stride, int V, int t_fir
   }
 }
 
-__global__ void pf_argmax_final(const float *pv, const int *pi, int t_first, int32_t *out_ids, int *last_id,
-                                int t_last) {
+__global__ void pf_argmax_final(const float *pv, const int *pi, int t_first, const PfCall *call, int t_last) {
   const int t = blockIdx.x, lane = threadIdx.x;
+  int32_t *out_ids = call->out_ids;
+  int *last_id = call->last_id;
   float v = -INFINITY;
   int i = 0x7fffffff;
   for (int b = lane; b < PF_ARGMAX_BLOCKS; b += 32)
@@ -321,6 +325,8 @@ __global__ void pf_argmax_final(const float *pv, const int *pi, int t_first, int
 // ---------------------------------------------------------------------------
 namespace mkp {
 namespace {
+
+constexpr size_t kBlasWorkspace = 32u << 20;   // bytes
 
 template <typename T>
 int dalloc(T **p, size_t n) {
@@ -365,9 +371,17 @@ int pf_init(PfState &st, int tc, int H, int Hq, int Hkv, int d, int I) {
       (rc = dalloc(&st.qkv3, 3 * T * rows)) || (rc = dalloc(&st.y3, 3 * T * H)) ||
       (rc = dalloc(&st.gate3, 3 * T * I)) || (rc = dalloc(&st.up3, 3 * T * I)) ||
       (rc = dalloc(&st.hs, 3 * T * kmax)) || (rc = dalloc(&st.pv, T * PF_ARGMAX_BLOCKS)) ||
-      (rc = dalloc(&st.pi, T * PF_ARGMAX_BLOCKS)) || (rc = dalloc(&st.err, 1))) {
+      (rc = dalloc(&st.pi, T * PF_ARGMAX_BLOCKS)) || (rc = dalloc(&st.err, 1)) || (rc = dalloc(&st.call, 1)) ||
+      (rc = dalloc(reinterpret_cast<unsigned char **>(&st.blas_ws), kBlasWorkspace))) {
     pf_free(st);
     return rc;
+  }
+  // a fixed workspace: the library then allocates nothing while a prefill is captured
+  if (cublasSetWorkspace(b, st.blas_ws, kBlasWorkspace) != CUBLAS_STATUS_SUCCESS ||
+      cudaStreamCreateWithFlags(&st.cap, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    pf_free(st);
+    return MK_ERR_CUDA;
   }
   st.tc = tc;
   st.kmax = kmax;
@@ -375,35 +389,29 @@ int pf_init(PfState &st, int tc, int H, int Hq, int Hkv, int d, int I) {
 }
 
 void pf_free(PfState &st) {
-  void *ps[] = {st.x, st.qkv, st.attn, st.qkv3, st.y3, st.gate3, st.up3, st.logits3, st.pv, st.pi, st.hs, st.err};
+  for (PfState::Graph &g : st.graphs) {
+    cudaGraphExecDestroy(g.exec);
+    cudaGraphDestroy(g.graph);
+  }
+  if (st.cap) cudaStreamDestroy(st.cap);
+  void *ps[] = {st.x,  st.qkv, st.attn, st.qkv3, st.y3, st.gate3,   st.up3,
+                st.logits3, st.pv, st.pi, st.hs, st.err, st.call, st.blas_ws};
   for (void *p : ps)
     if (p) cudaFree(p);
   if (st.blas) cublasDestroy(static_cast<cublasHandle_t>(st.blas));
   st = PfState();
 }
 
-int pf_run(PfState &st, PfArgs a, const PfLayer *layers, const uint16_t *final_norm, const uint16_t *lm_head,
-           int n, int32_t *out_ids, float *logits_out, int *last_id, cudaStream_t s) {
+// every launch of an n-token prefill, in order, on stream s
+int pf_enqueue(PfState &st, const PfArgs &a, const PfLayer *layers, const uint16_t *final_norm,
+               const uint16_t *lm_head, int n, bool all_logits, cudaStream_t s) {
   cublasHandle_t b = static_cast<cublasHandle_t>(st.blas);
   if (cublasSetStream(b, s) != CUBLAS_STATUS_SUCCESS) return MK_ERR_CUDA;
   const int rows = (a.Hq + 2 * a.Hkv) * a.d;
   const int grp = a.Hq / a.Hkv;
-  if ((a.d != 64 && a.d != 128) || a.Hq % a.Hkv || (grp != 1 && grp != 2 && grp != 4 && !(grp == 8 && a.d == 64)))
-    return MK_ERR_UNSUPPORTED;
   const size_t T = st.tc;
-  if (!st.logits3) {
-    int rc = dalloc(&st.logits3, 3 * T * a.V);
-    if (rc) return rc;
-  }
-  a.x = st.x; a.qkv = st.qkv; a.attn = st.attn;
-  a.qkv3 = st.qkv3; a.qkv_stride = T * rows;
-  a.y3 = st.y3; a.y_stride = T * a.H;
-  a.hs = st.hs; a.hs_stride = T * st.kmax;
-  a.err = st.err;
   const long long hs_s = static_cast<long long>(a.hs_stride);
   const long long ffn_s = static_cast<long long>(T) * a.I, lg_s = static_cast<long long>(T) * a.V;
-  if (cudaMemsetAsync(st.err, 0, sizeof(int), s) != cudaSuccess) return MK_ERR_CUDA;
-  const bool all_logits = out_ids || logits_out;
   int rc = MK_OK;
   for (int t0 = 0; t0 < n && rc == MK_OK; t0 += st.tc) {
     const int nt = n - t0 < st.tc ? n - t0 : st.tc;
@@ -458,11 +466,65 @@ int pf_run(PfState &st, PfArgs a, const PfLayer *layers, const uint16_t *final_n
       const size_t off = static_cast<size_t>(first) * a.H;
       if ((rc = gemm3(b, st.hs + off, hs_s, lm_head, m, a.V, a.H, st.logits3, a.V, lg_s))) break;
       pf_argmax_part<<<dim3(PF_ARGMAX_BLOCKS, m), PF_THREADS, 0, s>>>(st.logits3, static_cast<size_t>(lg_s), a.V,
-                                                                     t0 + first, logits_out, st.pv, st.pi, st.err);
-      pf_argmax_final<<<m, 32, 0, s>>>(st.pv, st.pi, t0 + first, out_ids, last_id, n - 1);
+                                                                     t0 + first, st.call, st.pv, st.pi, st.err);
+      pf_argmax_final<<<m, 32, 0, s>>>(st.pv, st.pi, t0 + first, st.call, n - 1);
     }
   }
   if (cudaGetLastError() != cudaSuccess && rc == MK_OK) rc = MK_ERR_CUDA;
+  return rc;
+}
+
+int pf_run(PfState &st, PfArgs a, const PfLayer *layers, const uint16_t *final_norm, const uint16_t *lm_head,
+           int n, const PfCall &call, cudaStream_t s) {
+  const int grp = a.Hq / a.Hkv;
+  if ((a.d != 64 && a.d != 128) || a.Hq % a.Hkv || (grp != 1 && grp != 2 && grp != 4 && !(grp == 8 && a.d == 64)))
+    return MK_ERR_UNSUPPORTED;
+  const size_t T = st.tc;
+  if (!st.logits3) {
+    int rc = dalloc(&st.logits3, 3 * T * a.V);
+    if (rc) return rc;
+  }
+  const int rows = (a.Hq + 2 * a.Hkv) * a.d;
+  a.x = st.x; a.qkv = st.qkv; a.attn = st.attn;
+  a.qkv3 = st.qkv3; a.qkv_stride = T * rows;
+  a.y3 = st.y3; a.y_stride = T * a.H;
+  a.hs = st.hs; a.hs_stride = T * st.kmax;
+  a.call = st.call;
+  a.err = st.err;
+  const bool all_logits = call.out_ids || call.logits_out;
+  // the call's fields, then the (captured once, replayed) launch sequence
+  if (cudaMemcpyAsync(st.call, &call, sizeof(PfCall), cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemsetAsync(st.err, 0, sizeof(int), s) != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
+  cudaGraphExec_t exec = nullptr;
+  for (const PfState::Graph &g : st.graphs)
+    if (g.n == n && g.all_logits == all_logits) exec = g.exec;
+  int rc = MK_OK;
+  if (!exec) {
+    cudaGraph_t graph = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(st.cap, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+      rc = pf_enqueue(st, a, layers, final_norm, lm_head, n, all_logits, st.cap);
+      const cudaError_t e2 = cudaStreamEndCapture(st.cap, &graph);
+      if (rc == MK_OK && e2 == cudaSuccess) e = cudaGraphInstantiate(&exec, graph, 0);
+      else e = e2 != cudaSuccess ? e2 : cudaErrorUnknown;
+    }
+    if (e == cudaSuccess && rc == MK_OK && exec) {
+      st.graphs.push_back(PfState::Graph{n, all_logits, graph, exec});
+    } else {
+      // not capturable here: run the same sequence directly
+      if (graph) cudaGraphDestroy(graph);
+      exec = nullptr;
+      cudaGetLastError();
+      rc = pf_enqueue(st, a, layers, final_norm, lm_head, n, all_logits, s);
+    }
+  }
+  if (exec && cudaGraphLaunch(exec, s) != cudaSuccess) {
+    cudaGetLastError();
+    rc = MK_ERR_CUDA;
+  }
   int herr = 0;
   if (cudaMemcpyAsync(&herr, st.err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess) {

@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cstddef>
 #include <cuda_runtime.h>
+#include <vector>
 
 #include "../../include/mk.h"
 
@@ -13,7 +14,22 @@ constexpr int MK_PF_ERR_BAD_TOKEN = MK_ERR_BAD_TOKEN;
 constexpr int MK_PF_ERR_NUMERIC = MK_ERR_NUMERIC;
 constexpr int MK_PF_ERR_BAD_POSITION = MK_ERR_BAD_POSITION;
 
-// everything a prefill kernel reads: shape, model, handle state, call, scratch
+// the call-dependent fields, read by the kernels from a device copy so that a
+// captured graph of the prefill can be replayed for another call
+struct PfCall {
+  const int32_t *ids;               // [n] prompt ids (device)
+  const float *embeds;              // sentinel rows [n_embed_rows][H] fp32, or NULL
+  int n_embed_rows;
+  const int32_t *pos3;              // [3][n_pos] position streams, or NULL
+  int n_pos, pos0;
+  float *hidden;                    // [n][L+1][H] or NULL
+  int32_t *out_ids;                 // [n] greedy ids, or NULL
+  float *logits_out;                // [n][V], or NULL
+  int *last_id;                     // the last token's greedy id (the handle's)
+};
+
+// everything a prefill kernel reads: shape, model, handle state, scratch, and
+// the device copy of the call
 struct PfArgs {
   int L, H, Hq, Hkv, d, I, V, vocab_in;
   float eps, inv_sqrt_d;
@@ -21,12 +37,7 @@ struct PfArgs {
   const uint16_t *embed;            // [vocab_in][H] bf16
   const float2 *rope;               // [rope_len][d/2] (cos, sin)
   uint16_t *kcache, *vcache;        // [L][Hkv][max_seq][d] bf16, the decode kernel's cache
-  const int32_t *ids;               // [n] prompt ids (device)
-  const float *embeds;              // sentinel rows [n_embed_rows][H] fp32, or NULL
-  int n_embed_rows;
-  const int32_t *pos3;              // [3][n_pos] position streams, or NULL
-  int n_pos, pos0;
-  float *hidden;                    // [n][L+1][H] or NULL
+  const PfCall *call;               // device copy of the call's fields
   int *err;                         // first error code (device)
   float *x, *qkv, *attn;            // chunk scratch (fp32): residual, normed q, attention output
   float *qkv3, *y3;                 // GEMM outputs as three partials, qkv_stride / y_stride apart
@@ -52,16 +63,27 @@ struct PfState {
   uint16_t *hs = nullptr;           // [3][tc][kmax] bf16 input terms
   size_t kmax = 0;
   int *err = nullptr;
+  PfCall *call = nullptr;           // device copy of the current call
+  void *blas_ws = nullptr;          // GEMM workspace (fixed, so the GEMMs can be captured)
+  cudaStream_t cap = nullptr;       // capture stream
+  struct Graph {
+    int n;
+    bool all_logits;
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+  };
+  std::vector<Graph> graphs;        // captured prefills, one per (n, all_logits)
 };
 
 int pf_init(PfState &st, int tc, int H, int Hq, int Hkv, int d, int I);
 void pf_free(PfState &st);
 
-// Run n prompt forwards (positions a.pos0 ..): fills the KV cache, writes
+// Run n prompt forwards (positions call.pos0 ..): fills the KV cache, writes
 // hidden / logits / out_ids when given, and the last token's greedy id to
-// *last_id (device).  Returns MK_OK or an MK_ERR_* code (after the stream
-// has completed).
+// *call.last_id (device).  The launch sequence of a given (n, all ids or not)
+// is captured as a CUDA graph on first use and replayed afterwards.  Returns
+// MK_OK or an MK_ERR_* code (after the stream has completed).
 int pf_run(PfState &st, PfArgs a, const PfLayer *layers, const uint16_t *final_norm, const uint16_t *lm_head,
-           int n, int32_t *out_ids, float *logits_out, int *last_id, cudaStream_t s);
+           int n, const PfCall &call, cudaStream_t s);
 
 }  // namespace mkp

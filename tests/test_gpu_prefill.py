@@ -82,6 +82,28 @@ def test_prefill_sentinel_rows():
     _prefill_then_decode("mid", 12, 4, 24, sentinel=True)
 
 
+def test_prefill_graph_replay_for_new_calls_and_positions():
+    # the launch sequence of a prompt length is captured once and replayed: a
+    # replay with other ids, another cursor and other output buffers must give
+    # what a first (capturing) call gives, and the oracle's prefix result
+    s = W.shape("mid")
+    w = W.make_weights(s, seed=0)
+    p1 = W.make_prompt(s["vocab_in"], 16, seed=1)
+    p2 = W.make_prompt(s["vocab_in"], 16, seed=7)
+    a = mk.Decoder(s, w, max_seq=40)
+    a.prefill(p1)                                   # captures the 16-token graph
+    la = torch.full((16, s["vocab"]), float("nan"), device="cuda:0")
+    ia = a.prefill(p2, logits=la).cpu().numpy()     # replay at position 16
+    b = mk.Decoder(s, w, max_seq=40)
+    b.prefill(p1, all_ids=False)                    # another graph (last id only)
+    lb = torch.full((16, s["vocab"]), float("nan"), device="cuda:0")
+    ib = b.prefill(p2, logits=lb).cpu().numpy()     # first all-ids call on b: captured now
+    torch.cuda.synchronize()
+    assert np.array_equal(ia, ib) and torch.equal(la, lb)
+    pl, _, _, _ = O.prefix_forward(s, w, np.concatenate([p1, p2]))
+    assert_close(la.double().cpu().numpy(), pl[16:], "replayed prefill at position 16")
+
+
 def test_prefill_last_id_only_and_errors():
     # without ids only the last token's logits are computed; decode continues
     # from its greedy id exactly as after a one-token-per-forward prompt
