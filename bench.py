@@ -36,21 +36,26 @@ CSRC = os.path.join(ROOT, "persistent_transformer_megakernel_gb300", "csrc")
 PROFILES = os.path.join(ROOT, "profiles")
 
 
+# the files the decode kernel and its launch are built from; the prefill and
+# embedding kernels do not change what the decode kernel reads or writes
+DECODE_SOURCES = ("mk_device.cuh", "mk_host.cu", "mk_kernels_d128.cu", "mk_kernels_d64.cu", "mk_launch.h",
+                  "mk_params.h", "ptx.cuh")
+
+
 def kernel_sources_sha256():
-    import glob
     import hashlib
     h = hashlib.sha256()
-    for path in sorted(glob.glob(os.path.join(CSRC, "*"))):
-        h.update(os.path.basename(path).encode())
-        with open(path, "rb") as f:
+    for name in sorted(DECODE_SOURCES):
+        h.update(name.encode())
+        with open(os.path.join(CSRC, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
 def measured_traffic(workload, forwards_per_launch):
     """DRAM bytes (read + write) per launch from the ncu record of this
-    workload, scaled by forwards; None when there is no record or the kernel
-    sources changed since it was taken."""
+    workload, scaled by forwards; None when there is no record or the decode
+    kernel's sources changed since it was taken."""
     path = os.path.join(PROFILES, "traffic_%s.json" % workload)
     try:
         with open(path) as f:

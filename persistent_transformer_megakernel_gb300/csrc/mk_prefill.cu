@@ -202,54 +202,223 @@ __global__ void pf_qk_rope_append(const PfArgs a, int layer, const uint16_t *q_n
   }
 }
 
-// Causal GQA attention of the chunk's tokens over the cache: one warp per
-// (token, kv head) handles the GRP query heads that read that kv head, with
-// an online softmax over slots 0..P (running max m, sum l, output o).
+// Causal GQA attention of the chunk's tokens over the cache, tiled so that
+// every cached K / V row read from memory serves many query rows.  A CTA owns
+// one kv head g and PF_AR query rows (the GRP heads that read g, for
+// PF_AR / GRP consecutive tokens); it walks the cache in tiles of PF_AP
+// positions, slots 0 .. the last row's position, with an online softmax per
+// row (running max m, sum l, output o).  A tile's K and V rows are widened to
+// fp32 in shared memory; the scores q . k are formed in 2 x 4 register blocks
+// (rows x positions), the weights e^(s - m) go through shared memory, and the
+// output update o <- c o + sum_p w_p V[p] runs in 4-row register blocks.
+// Position p of row r is masked (weight 0) when p exceeds r's own position.
+// Loads of the next tile are issued before the current tile is computed.
+constexpr int PF_AR = 32;                   // query rows per CTA
+constexpr int PF_AP = 64;                   // cached positions per tile
+constexpr int PF_KPAD = 4;                  // K / Q row padding (floats): conflict-free float4 reads
+constexpr int PF_PPAD = 16;                 // weight row padding: the two rows of a warp in distinct banks
+
+template <int HD>
+constexpr size_t pf_attention_smem() {
+  return sizeof(float) * (static_cast<size_t>(PF_AR) * (HD + PF_KPAD) + static_cast<size_t>(PF_AP) * (HD + PF_KPAD) +
+                          static_cast<size_t>(PF_AP) * HD + static_cast<size_t>(PF_AR) * (PF_AP + PF_PPAD) + 2 * PF_AR);
+}
+
 template <int HD, int GRP>
-__global__ void pf_attention(const PfArgs a, int layer, int t0, int nt) {
-  constexpr int EPL = HD / 32;
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (warp >= nt * a.Hkv) return;
-  const int t = warp / a.Hkv, g = warp % a.Hkv;
-  const int P = a.call->pos0 + t0 + t;
+__global__ void __launch_bounds__(PF_THREADS) pf_attention(const PfArgs a, int layer, int t0, int nt) {
+  static_assert(PF_THREADS == 256 && PF_AR == 32 && PF_AP == 64, "thread mappings below assume these sizes");
+  static_assert(PF_AR % GRP == 0, "a CTA holds whole tokens");
+  constexpr int TT = PF_AR / GRP;           // tokens per CTA
+  constexpr int QS = HD + PF_KPAD;          // row stride of Qs and Ks (floats)
+  constexpr int PS = PF_AP + PF_PPAD;       // row stride of Ps
+  constexpr int C8 = HD / 8;                // 16-byte pieces of a cached bf16 row
+  constexpr int NLD = PF_AP * C8 / PF_THREADS;   // pieces per thread per tile (K and V each)
+  constexpr int CPT = HD / 32;              // output columns per thread
+  static_assert(NLD * PF_THREADS == PF_AP * C8, "tile pieces divide among the threads");
+  extern __shared__ __align__(16) float sm[];
+  float *Qs = sm;                           // [PF_AR][QS]
+  float *Ks = Qs + PF_AR * QS;              // [PF_AP][QS]
+  float *Vs = Ks + PF_AP * QS;              // [PF_AP][HD]
+  float *Ps = Vs + PF_AP * HD;              // [PF_AR][PS]
+  float *Cs = Ps + PF_AR * PS;              // [PF_AR] rescale factor of the tile
+  float *Ls = Cs + PF_AR;                   // [PF_AR] final softmax sums
+
+  const int tid = threadIdx.x;
+  const int g = blockIdx.y;
+  const int tok0 = blockIdx.x * TT;
+  const int ntok = min(TT, nt - tok0);
+  const int base_pos = a.call->pos0 + t0;
+  const int pmax = base_pos + tok0 + ntok - 1;         // the CTA's last cached slot
   const int rows = (a.Hq + 2 * a.Hkv) * HD;
-  float q[GRP][EPL], o[GRP][EPL], m[GRP], l[GRP];
-#pragma unroll
-  for (int h = 0; h < GRP; ++h) {
-    const float *qs = a.qkv + static_cast<size_t>(t) * rows + static_cast<size_t>(g * GRP + h) * HD;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) { q[h][e] = qs[lane + 32 * e]; o[h][e] = 0.f; }
-    m[h] = -INFINITY;
-    l[h] = 0.f;
+
+  // queries: row r = token tok0 + r / GRP, head g * GRP + r % GRP; rows past the
+  // chunk hold zeros (and read slot 0 only; never stored)
+  for (int e = tid; e < PF_AR * HD / 4; e += PF_THREADS) {
+    const int r = e / (HD / 4), c4 = e % (HD / 4);
+    const int tt = r / GRP, h = r % GRP;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tt < ntok)
+      v = *reinterpret_cast<const float4 *>(a.qkv + static_cast<size_t>(tok0 + tt) * rows +
+                                            static_cast<size_t>(g * GRP + h) * HD + 4 * c4);
+    *reinterpret_cast<float4 *>(Qs + r * QS + 4 * c4) = v;
   }
+
   const uint16_t *kb = a.kcache + (static_cast<size_t>(layer) * a.Hkv + g) * a.max_seq * HD;
   const uint16_t *vb = a.vcache + (static_cast<size_t>(layer) * a.Hkv + g) * a.max_seq * HD;
-  for (int pos = 0; pos <= P; ++pos) {
-    float kk[EPL], vv[EPL];
+  uint4 kreg[NLD], vreg[NLD];
+  // a tile's rows past pmax are zeros: never read (they may hold stale or unset bits)
+  auto load_tile = [&](int pb) {
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      kk[e] = bf2f(kb[static_cast<size_t>(pos) * HD + lane + 32 * e]);
-      vv[e] = bf2f(vb[static_cast<size_t>(pos) * HD + lane + 32 * e]);
+    for (int u = 0; u < NLD; ++u) {
+      const int e = tid + u * PF_THREADS;
+      const int pp = pb + e / C8, c8 = e % C8;
+      kreg[u] = make_uint4(0u, 0u, 0u, 0u);
+      vreg[u] = kreg[u];
+      if (pp <= pmax) {
+        kreg[u] = *reinterpret_cast<const uint4 *>(kb + static_cast<size_t>(pp) * HD + 8 * c8);
+        vreg[u] = *reinterpret_cast<const uint4 *>(vb + static_cast<size_t>(pp) * HD + 8 * c8);
+      }
     }
+  };
+  auto store_tile = [&]() {
 #pragma unroll
-    for (int h = 0; h < GRP; ++h) {
-      float s = 0.f;
+    for (int u = 0; u < NLD; ++u) {
+      const int e = tid + u * PF_THREADS;
+      const int pl = e / C8, c8 = e % C8;
+      const uint4 k = kreg[u], v = vreg[u];
+      float *kd = Ks + pl * QS + 8 * c8;
+      float *vd = Vs + pl * HD + 8 * c8;
+      *reinterpret_cast<float4 *>(kd) = make_float4(__uint_as_float(k.x << 16), __uint_as_float(k.x & 0xffff0000u),
+                                                    __uint_as_float(k.y << 16), __uint_as_float(k.y & 0xffff0000u));
+      *reinterpret_cast<float4 *>(kd + 4) = make_float4(__uint_as_float(k.z << 16), __uint_as_float(k.z & 0xffff0000u),
+                                                        __uint_as_float(k.w << 16), __uint_as_float(k.w & 0xffff0000u));
+      *reinterpret_cast<float4 *>(vd) = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                                                    __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+      *reinterpret_cast<float4 *>(vd + 4) = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u),
+                                                        __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+    }
+  };
+
+  // score mapping: rows ty, ty + 16; positions tx + 16 j (a row's 16 threads are
+  // one half-warp)
+  const int ty = tid >> 4, tx = tid & 15;
+  int prow[2];
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) s = fmaf(q[h][e], kk[e], s);
-      s = warp_sum(s);
-      const float mn = fmaxf(m[h], s);
-      const float c = expf(m[h] - mn), w = expf(s - mn);
-      l[h] = l[h] * c + w;
+  for (int i = 0; i < 2; ++i) {
+    const int tt = (ty + 16 * i) / GRP;
+    prow[i] = tt < ntok ? base_pos + tok0 + tt : 0;
+  }
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  // output mapping: rows oy + 8 i, columns CPT * ox ..
+  const int oy = tid >> 5, ox = tid & 31;
+  float o[4][CPT];
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) o[h][e] = fmaf(w, vv[e], o[h][e] * c);
-      m[h] = mn;
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) o[i][c] = 0.f;
+
+  const int ntiles = pmax / PF_AP + 1;
+  load_tile(0);
+  store_tile();
+  __syncthreads();
+  for (int ti = 0; ti < ntiles; ++ti) {
+    const int pb = ti * PF_AP;
+    if (ti + 1 < ntiles) load_tile(pb + PF_AP);
+    // ---- scores of this tile ----------------------------------------------
+    float s[2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s[i][j] = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < HD; k += 4) {
+      const float4 q0 = *reinterpret_cast<const float4 *>(Qs + ty * QS + k);
+      const float4 q1 = *reinterpret_cast<const float4 *>(Qs + (ty + 16) * QS + k);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 kv = *reinterpret_cast<const float4 *>(Ks + (tx + 16 * j) * QS + k);
+        s[0][j] = fmaf(q0.x, kv.x, fmaf(q0.y, kv.y, fmaf(q0.z, kv.z, fmaf(q0.w, kv.w, s[0][j]))));
+        s[1][j] = fmaf(q1.x, kv.x, fmaf(q1.y, kv.y, fmaf(q1.z, kv.z, fmaf(q1.w, kv.w, s[1][j]))));
+      }
+    }
+    // ---- online softmax, per row over its half-warp -------------------------
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (pb + tx + 16 * j > prow[i]) s[i][j] = -INFINITY;
+        mx = fmaxf(mx, s[i][j]);
+      }
+#pragma unroll
+      for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      // slot 0 is in every row's range, so m is finite after the first tile
+      const float mn = fmaxf(m[i], mx);
+      const float c = expf(m[i] - mn);
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float w = s[i][j] == -INFINITY ? 0.f : expf(s[i][j] - mn);
+        Ps[(ty + 16 * i) * PS + tx + 16 * j] = w;
+        sum += w;
+      }
+#pragma unroll
+      for (int off = 8; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      l[i] = l[i] * c + sum;
+      m[i] = mn;
+      if (tx == 0) Cs[ty + 16 * i] = c;
+    }
+    __syncthreads();
+    // ---- o <- c o + sum_p w_p V[p] ------------------------------------------
+    float cr[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cr[i] = Cs[oy + 8 * i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) o[i][c] *= cr[i];
+#pragma unroll 2
+    for (int p = 0; p < PF_AP; p += 4) {
+      float4 w4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w4[i] = *reinterpret_cast<const float4 *>(Ps + (oy + 8 * i) * PS + p);
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        float v[CPT];
+        if constexpr (CPT == 4) {
+          const float4 t = *reinterpret_cast<const float4 *>(Vs + (p + qq) * HD + 4 * ox);
+          v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+        } else {
+          const float2 t = *reinterpret_cast<const float2 *>(Vs + (p + qq) * HD + 2 * ox);
+          v[0] = t.x; v[1] = t.y;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float w = qq == 0 ? w4[i].x : qq == 1 ? w4[i].y : qq == 2 ? w4[i].z : w4[i].w;
+#pragma unroll
+          for (int c = 0; c < CPT; ++c) o[i][c] = fmaf(w, v[c], o[i][c]);
+        }
+      }
+    }
+    __syncthreads();
+    if (ti + 1 < ntiles) {
+      store_tile();
+      __syncthreads();
     }
   }
+  if (tx == 0) {
+    Ls[ty] = l[0];
+    Ls[ty + 16] = l[1];
+  }
+  __syncthreads();
 #pragma unroll
-  for (int h = 0; h < GRP; ++h) {
-    float *dst = a.attn + static_cast<size_t>(t) * a.Hq * HD + static_cast<size_t>(g * GRP + h) * HD;
+  for (int i = 0; i < 4; ++i) {
+    const int r = oy + 8 * i, tt = r / GRP, h = r % GRP;
+    if (tt >= ntok) continue;
+    const float inv = 1.0f / Ls[r];
+    float *dst = a.attn + static_cast<size_t>(tok0 + tt) * a.Hq * HD + static_cast<size_t>(g * GRP + h) * HD + CPT * ox;
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) dst[lane + 32 * e] = o[h][e] / l[h];
+    for (int c = 0; c < CPT; ++c) dst[c] = o[i][c] * inv;
   }
 }
 
@@ -355,6 +524,25 @@ int blocks_for(size_t n) { return static_cast<int>((n + PF_THREADS - 1) / PF_THR
 
 }  // namespace
 
+// one CTA per (kv head, PF_AR query rows); the dynamic shared memory above
+// 48 KB is enabled once per instantiation by pf_attention_enable
+template <int HD, int GRP>
+void launch_attention(const PfArgs &a, int layer, int t0, int nt, cudaStream_t s) {
+  constexpr int TT = PF_AR / GRP;
+  pf_attention<HD, GRP><<<dim3((nt + TT - 1) / TT, a.Hkv), PF_THREADS, pf_attention_smem<HD>(), s>>>(a, layer, t0, nt);
+}
+
+template <int HD, int GRP>
+bool attention_attr() {
+  return cudaFuncSetAttribute(pf_attention<HD, GRP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(pf_attention_smem<HD>())) == cudaSuccess;
+}
+
+bool pf_attention_enable() {
+  return attention_attr<64, 1>() && attention_attr<64, 2>() && attention_attr<64, 4>() && attention_attr<64, 8>() &&
+         attention_attr<128, 1>() && attention_attr<128, 2>() && attention_attr<128, 4>();
+}
+
 int pf_init(PfState &st, int tc, int H, int Hq, int Hkv, int d, int I) {
   if (st.tc >= tc) return MK_OK;
   pf_free(st);
@@ -378,7 +566,7 @@ int pf_init(PfState &st, int tc, int H, int Hq, int Hkv, int d, int I) {
   }
   // a fixed workspace: the library then allocates nothing while a prefill is captured
   if (cublasSetWorkspace(b, st.blas_ws, kBlasWorkspace) != CUBLAS_STATUS_SUCCESS ||
-      cudaStreamCreateWithFlags(&st.cap, cudaStreamNonBlocking) != cudaSuccess) {
+      cudaStreamCreateWithFlags(&st.cap, cudaStreamNonBlocking) != cudaSuccess || !pf_attention_enable()) {
     cudaGetLastError();
     pf_free(st);
     return MK_ERR_CUDA;
@@ -425,22 +613,22 @@ int pf_enqueue(PfState &st, const PfArgs &a, const PfLayer *layers, const uint16
           (rc = gemm3(b, st.hs, hs_s, w.wv, nt, a.Hkv * a.d, a.H, st.qkv3 + (a.Hq + a.Hkv) * a.d, rows,
                       a.qkv_stride)))
         break;
-      const int jobs_warps = nt * (a.Hq + 2 * a.Hkv), attn_warps = nt * a.Hkv;
+      const int jobs_warps = nt * (a.Hq + 2 * a.Hkv);
       const int wpb = PF_THREADS / 32;
       if (a.d == 64) {
         pf_qk_rope_append<64><<<(jobs_warps + wpb - 1) / wpb, PF_THREADS, 0, s>>>(a, l, w.q_norm, w.k_norm, t0, nt);
         switch (grp) {
-          case 1: pf_attention<64, 1><<<(attn_warps + wpb - 1) / wpb, PF_THREADS, 0, s>>>(a, l, t0, nt); break;
-          case 2: pf_attention<64, 2><<<(attn_warps + wpb - 1) / wpb, PF_THREADS, 0, s>>>(a, l, t0, nt); break;
-          case 4: pf_attention<64, 4><<<(attn_warps + wpb - 1) / wpb, PF_THREADS, 0, s>>>(a, l, t0, nt); break;
-          default: pf_attention<64, 8><<<(attn_warps + wpb - 1) / wpb, PF_THREADS, 0, s>>>(a, l, t0, nt); break;
+          case 1: launch_attention<64, 1>(a, l, t0, nt, s); break;
+          case 2: launch_attention<64, 2>(a, l, t0, nt, s); break;
+          case 4: launch_attention<64, 4>(a, l, t0, nt, s); break;
+          default: launch_attention<64, 8>(a, l, t0, nt, s); break;
         }
       } else {
         pf_qk_rope_append<128><<<(jobs_warps + wpb - 1) / wpb, PF_THREADS, 0, s>>>(a, l, w.q_norm, w.k_norm, t0, nt);
         switch (grp) {
-          case 1: pf_attention<128, 1><<<(attn_warps + wpb - 1) / wpb, PF_THREADS, 0, s>>>(a, l, t0, nt); break;
-          case 2: pf_attention<128, 2><<<(attn_warps + wpb - 1) / wpb, PF_THREADS, 0, s>>>(a, l, t0, nt); break;
-          default: pf_attention<128, 4><<<(attn_warps + wpb - 1) / wpb, PF_THREADS, 0, s>>>(a, l, t0, nt); break;
+          case 1: launch_attention<128, 1>(a, l, t0, nt, s); break;
+          case 2: launch_attention<128, 2>(a, l, t0, nt, s); break;
+          default: launch_attention<128, 4>(a, l, t0, nt, s); break;
         }
       }
       pf_split<<<blocks_for(static_cast<size_t>(nt) * a.Hq * a.d), PF_THREADS, 0, s>>>(st.attn, a.Hq * a.d, nt,
