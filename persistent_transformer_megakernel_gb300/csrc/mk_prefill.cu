@@ -539,8 +539,8 @@ bool attention_attr() {
 }
 
 bool pf_attention_enable() {
-  return attention_attr<64, 1>() && attention_attr<64, 2>() && attention_attr<64, 4>() && attention_attr<64, 8>() &&
-         attention_attr<128, 1>() && attention_attr<128, 2>() && attention_attr<128, 4>();
+  return attention_attr<64, 1>() && attention_attr<64, 2>() && attention_attr<64, 4>() && attention_attr<128, 1>() &&
+         attention_attr<128, 2>();
 }
 
 int pf_init(PfState &st, int tc, int H, int Hq, int Hkv, int d, int I) {
@@ -617,18 +617,17 @@ int pf_enqueue(PfState &st, const PfArgs &a, const PfLayer *layers, const uint16
       const int wpb = PF_THREADS / 32;
       if (a.d == 64) {
         pf_qk_rope_append<64><<<(jobs_warps + wpb - 1) / wpb, PF_THREADS, 0, s>>>(a, l, w.q_norm, w.k_norm, t0, nt);
+        // groups mk_create accepts: group * head_dim <= 256
         switch (grp) {
           case 1: launch_attention<64, 1>(a, l, t0, nt, s); break;
           case 2: launch_attention<64, 2>(a, l, t0, nt, s); break;
-          case 4: launch_attention<64, 4>(a, l, t0, nt, s); break;
-          default: launch_attention<64, 8>(a, l, t0, nt, s); break;
+          default: launch_attention<64, 4>(a, l, t0, nt, s); break;
         }
       } else {
         pf_qk_rope_append<128><<<(jobs_warps + wpb - 1) / wpb, PF_THREADS, 0, s>>>(a, l, w.q_norm, w.k_norm, t0, nt);
         switch (grp) {
           case 1: launch_attention<128, 1>(a, l, t0, nt, s); break;
-          case 2: launch_attention<128, 2>(a, l, t0, nt, s); break;
-          default: launch_attention<128, 4>(a, l, t0, nt, s); break;
+          default: launch_attention<128, 2>(a, l, t0, nt, s); break;
         }
       }
       pf_split<<<blocks_for(static_cast<size_t>(nt) * a.Hq * a.d), PF_THREADS, 0, s>>>(st.attn, a.Hq * a.d, nt,

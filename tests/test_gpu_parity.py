@@ -57,6 +57,8 @@ def _teacher_forced(name, n_prompt, n_steps, max_seq=64, pos3_mode=None, per_op=
     ("tiny", 8, 16),          # the tiny oracle-check workload
     ("mid", 5, 70),           # 0.6B-wide layers: several tiles per CTA, ragged vocab, 75 positions
     ("gqa4", 6, 20),          # group 4, head_dim 64, tied head
+    ("mha", 6, 20),           # group 1 (multi-head attention), head_dim 128
+    ("mha64", 5, 24),         # group 1, head_dim 64, attention width 384 != hidden, tied head
 ])
 def test_teacher_forced_parity(name, n_prompt, n_steps):
     _teacher_forced(name, n_prompt, n_steps, max_seq=n_prompt + n_steps + 4)

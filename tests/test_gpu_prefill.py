@@ -68,6 +68,8 @@ def _prefill_then_decode(name, T, n_steps, max_seq, pos3_mode=None, sentinel=Fal
     ("mid", 40, 12, 64),        # 0.6B-wide layers
     ("gqa4", 20, 8, 40),        # group 4, head_dim 64, tied head
     ("tiny", 300, 4, 320),      # two chunks of the 256-token scratch
+    ("mha", 70, 6, 96),         # group 1, head_dim 128: three query tiles, two cache tiles
+    ("mha64", 100, 4, 128),     # group 1, head_dim 64, ragged last query tile
 ])
 def test_prefill_parity(name, T, n_steps, max_seq):
     _prefill_then_decode(name, T, n_steps, max_seq)

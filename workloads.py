@@ -67,6 +67,13 @@ SHAPES = {
     "mrope_small_interleaved": dict(n_layers=2, hidden=512, n_q_heads=8, n_kv_heads=4, head_dim=64,
                                     intermediate=1536, vocab=1024, vocab_in=1024, tied=False,
                                     mrope_sections=(12, 10, 10), mrope_interleaved=True),
+    # multi-head attention (GQA group 1, the degenerate case), head_dim 128 and 64
+    "mha": dict(n_layers=2, hidden=512, n_q_heads=4, n_kv_heads=4, head_dim=128,
+                intermediate=1536, vocab=2003, vocab_in=2003, tied=False,
+                mrope_sections=None),
+    "mha64": dict(n_layers=2, hidden=512, n_q_heads=6, n_kv_heads=6, head_dim=64,
+                  intermediate=1536, vocab=1024, vocab_in=1024, tied=True,
+                  mrope_sections=None),
 }
 
 #: fixed scalars of every shape (Qwen3 defaults)
