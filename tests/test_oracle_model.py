@@ -93,6 +93,46 @@ def test_attention_hand_example_two_positions():
     assert np.array_equal(dec.K[0, 0, 1], k1)
 
 
+def test_norm_gains_rotation_order_and_value_rounding_hand_example():
+    # One layer, d = 2 (one rotary pair, omega = 1), eps 0.  attn_norm = (1, 1),
+    # q_norm = (1, 2), k_norm = (2, 1): QK-norm is applied before the rotation,
+    # queries and keys with their own gains.  Wq = Wk = Wo = I,
+    # Wv = [[1, -2^-9], [0, 1/2]].  mlp_norm = (2, 1/2), gate row (1, 0), up row
+    # (0, 1), down column (1, 0): x += (silu(h0) h1, 0) with h = rmsnorm(x) (2, 1/2).
+    # step 0, x = (1, 1): h = (1, 1); v = (1 - 2^-9, 1/2) is cached in bf16 as
+    #   (1, 1/2) (1 - 2^-9 is the midpoint of 1 - 2^-8 and 1: ties to even);
+    #   one key, so o = (1, 1/2) and x = (2, 3/2); then the MLP with rms sqrt(3.125).
+    # step 1, x = (1, -1): h = (1, -1); q = R(1)(1, -2) = (c + 2s, s - 2c),
+    #   k1 = bf16(R(1)(2, -1)) = bf16((2c + s, 2s - c)), k0 = (2, 1);
+    #   v1 = bf16((1 + 2^-9, -1/2)) = (1, -1/2); scores q.k / sqrt2.
+    s = _shape()
+    lw = _layer(wv=[[1, -2.0 ** -9], [0, 0.5]], wo=np.eye(2), q_norm=[1, 2], k_norm=[2, 1],
+                mlp_norm=[2, 0.5], w_gate=[[1, 0]], w_up=[[0, 1]], w_down=[[1], [0]])
+    w = {"embed": _bits([[1, 1], [1, -1], [0, 0]]), "final_norm": _bits([1, 1]),
+         "lm_head": _bits([[1, 0], [0, 1], [1, 1]]), "layers": [lw]}
+
+    def mlp(x):
+        r = math.sqrt((x[0] ** 2 + x[1] ** 2) / 2)
+        h0, h1 = 2 * x[0] / r, 0.5 * x[1] / r
+        return np.array([x[0] + h0 / (1 + math.exp(-h0)) * h1, x[1]])
+
+    dec = O.Decoder(s, w, max_seq=4)
+    _, hid0 = dec.forward_embedding(O.bf16_bits_to_f64(w["embed"][0]))
+    assert np.array_equal(dec.V[0, 0, 0], [1.0, 0.5])
+    assert np.allclose(hid0[1], mlp(np.array([2.0, 1.5])), rtol=0, atol=1e-14)
+    _, hid1 = dec.forward_embedding(O.bf16_bits_to_f64(w["embed"][1]))
+    c, sn = math.cos(1.0), math.sin(1.0)
+    q = np.array([c + 2 * sn, sn - 2 * c])
+    k0 = np.array([2.0, 1.0])
+    k1 = _bf16([2 * c + sn, 2 * sn - c])
+    s0, s1 = float(q @ k0) / math.sqrt(2), float(q @ k1) / math.sqrt(2)
+    a0 = 1.0 / (1.0 + math.exp(s1 - s0))
+    o = a0 * np.array([1.0, 0.5]) + (1.0 - a0) * np.array([1.0, -0.5])
+    assert np.array_equal(dec.K[0, 0, 1], k1)
+    assert np.array_equal(dec.V[0, 0, 1], [1.0, -0.5])
+    assert np.allclose(hid1[1], mlp(np.array([1.0, -1.0]) + o), rtol=0, atol=1e-14)
+
+
 def test_final_norm_and_head_hand_example():
     # x = (3, 4): RMS sqrt(12.5); gain (1, 2) -> (3, 8)/sqrt(12.5) = (0.8485, 2.2627);
     # head rows (1,0), (0,1), (1,1) -> logits (0.8485, 2.2627, 3.1113); argmax 2.
