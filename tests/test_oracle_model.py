@@ -133,6 +133,50 @@ def test_norm_gains_rotation_order_and_value_rounding_hand_example():
     assert np.allclose(hid1[1], mlp(np.array([1.0, -1.0]) + o), rtol=0, atol=1e-14)
 
 
+def test_eps_inside_every_model_norm_hand_example():
+    # eps = 3 (large on purpose), one layer, d = 2, unit norm gains except the
+    # final norm (1, 2).  Wq = Wk = Wv = Wo = I; gate row (1, 0), up row (0, 2),
+    # down column (1, -1).  Every RMSNorm is x / sqrt(mean(x^2) + 3) * gain.
+    # step 0, x = (1, 1): h = (1, 1)/2; one key, so o = v = (1/2, 1/2), x = (3/2, 3/2).
+    # step 1, x = (1, -1): h = (1, -1)/2; q = k = R(1)((1, -1)/2 / sqrt(1/4 + 3));
+    #   k0 = bf16((1, 1)/2 / sqrt(3.25)), k1 = bf16(k); v0 = (1/2, 1/2), v1 = (1/2, -1/2).
+    # After attention: m = rmsnorm(x), x += (silu(m0) 2 m1, -silu(m0) 2 m1);
+    # logits = head . (x / sqrt(mean(x^2) + 3) * (1, 2)).
+    e = 3.0
+    s = _shape(rms_eps=e)
+    lw = _layer(wv=np.eye(2), wo=np.eye(2), w_gate=[[1, 0]], w_up=[[0, 2]], w_down=[[1], [-1]])
+    head = np.array([[1, 0], [0, 1], [1, 1]], dtype=float)
+    w = {"embed": _bits([[1, 1], [1, -1], [0, 0]]), "final_norm": _bits([1, 2]),
+         "lm_head": _bits(head), "layers": [lw]}
+
+    def rn(x):
+        return np.asarray(x) / math.sqrt(float(np.mean(np.square(x))) + e)
+
+    def after_attention(x):
+        m = rn(x)
+        u = m[0] / (1 + math.exp(-m[0])) * 2 * m[1]
+        return x + np.array([u, -u])
+
+    dec = O.Decoder(s, w, max_seq=4)
+    lg0, hid0 = dec.forward_embedding(O.bf16_bits_to_f64(w["embed"][0]))
+    x0 = after_attention(np.array([1.5, 1.5]))
+    assert np.allclose(hid0[1], x0, rtol=0, atol=1e-14)
+    assert np.allclose(lg0, head @ (rn(x0) * np.array([1.0, 2.0])), rtol=0, atol=1e-14)
+    lg1, hid1 = dec.forward_embedding(O.bf16_bits_to_f64(w["embed"][1]))
+    c, sn = math.cos(1.0), math.sin(1.0)
+    kn = np.array([0.5, -0.5]) / math.sqrt(0.25 + e)
+    q = np.array([kn[0] * c - kn[1] * sn, kn[1] * c + kn[0] * sn])
+    k0 = _bf16(np.array([0.5, 0.5]) / math.sqrt(0.25 + e))
+    k1 = _bf16(q)
+    s0, s1 = float(q @ k0) / math.sqrt(2), float(q @ k1) / math.sqrt(2)
+    a0 = 1.0 / (1.0 + math.exp(s1 - s0))
+    o = a0 * np.array([0.5, 0.5]) + (1.0 - a0) * np.array([0.5, -0.5])
+    x1 = after_attention(np.array([1.0, -1.0]) + o)
+    assert np.array_equal(dec.K[0, 0, 0], k0) and np.array_equal(dec.K[0, 0, 1], k1)
+    assert np.allclose(hid1[1], x1, rtol=0, atol=1e-14)
+    assert np.allclose(lg1, head @ (rn(x1) * np.array([1.0, 2.0])), rtol=0, atol=1e-14)
+
+
 def test_final_norm_and_head_hand_example():
     # x = (3, 4): RMS sqrt(12.5); gain (1, 2) -> (3, 8)/sqrt(12.5) = (0.8485, 2.2627);
     # head rows (1,0), (0,1), (1,1) -> logits (0.8485, 2.2627, 3.1113); argmax 2.

@@ -131,6 +131,20 @@ MUTATIONS = [
                                           "u = silu(lw[\"w_up\"] @ h) * (lw[\"w_gate\"] @ h)"),
                                          ("U = silu(Hn @ lw[\"w_gate\"].T) * (Hn @ lw[\"w_up\"].T)",
                                           "U = silu(Hn @ lw[\"w_up\"].T) * (Hn @ lw[\"w_gate\"].T)")]),
+    ("both: eps dropped from the layer and final norms",
+     [("h = rms_norm(x, lw[\"attn_norm\"], s.rms_eps)", "h = rms_norm(x, lw[\"attn_norm\"], 0.0)"),
+      ("h = rms_norm(x, lw[\"mlp_norm\"], s.rms_eps)", "h = rms_norm(x, lw[\"mlp_norm\"], 0.0)"),
+      ("logits = W.lm_head @ rms_norm(x, W.final_norm, s.rms_eps)",
+       "logits = W.lm_head @ rms_norm(x, W.final_norm, 0.0)"),
+      ("Hn = rms_norm(X, lw[\"attn_norm\"], s.rms_eps)", "Hn = rms_norm(X, lw[\"attn_norm\"], 0.0)"),
+      ("Hn = rms_norm(X, lw[\"mlp_norm\"], s.rms_eps)", "Hn = rms_norm(X, lw[\"mlp_norm\"], 0.0)"),
+      ("logits = rms_norm(X[rows], W.final_norm, s.rms_eps) @ W.lm_head.T",
+       "logits = rms_norm(X[rows], W.final_norm, 0.0) @ W.lm_head.T")]),
+    ("both: eps dropped from QK-norm",
+     [("q = rms_norm(q, lw[\"q_norm\"], s.rms_eps)", "q = rms_norm(q, lw[\"q_norm\"], 0.0)"),
+      ("k = rms_norm(k, lw[\"k_norm\"], s.rms_eps)", "k = rms_norm(k, lw[\"k_norm\"], 0.0)"),
+      ("rms_norm(Q, lw[\"q_norm\"], s.rms_eps)", "rms_norm(Q, lw[\"q_norm\"], 0.0)"),
+      ("rms_norm(Kx, lw[\"k_norm\"], s.rms_eps)", "rms_norm(Kx, lw[\"k_norm\"], 0.0)")]),
     ("both: final norm dropped", [("logits = W.lm_head @ rms_norm(x, W.final_norm, s.rms_eps)", "logits = W.lm_head @ x"),
                                   ("logits = rms_norm(X[rows], W.final_norm, s.rms_eps) @ W.lm_head.T",
                                    "logits = X[rows] @ W.lm_head.T")]),
