@@ -430,6 +430,8 @@ int mk_reset_kv(mk_handle *h, mk_stream stream) {
 int mk_decode_start(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_steps, int32_t *d_out_ids,
                     const mk_decode_opts *opts, mk_stream stream) {
   if (!h || h->pending || n_in < 0 || n_steps < 0) return MK_ERR_INVALID_ARG;
+  // forwards counted in 64 bits: two int32 counts may not fit an int together
+  if (static_cast<int64_t>(h->pos) + n_in + n_steps > h->cfg.max_seq) return MK_ERR_KV_FULL;
   const int n_fwd = n_in + n_steps;
   if (n_fwd == 0) {
     h->pending = 1;
@@ -449,7 +451,6 @@ int mk_decode_start(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t
   if (o.codes && (o.embeds || o.n_books < 0 || o.n_books > 64 || (o.n_books > 0 && (!o.books || o.book_rows < 1)) ||
                   !o.text || o.text_rows < 1 || !o.text_ids || o.n_code_rows < 0))
     return MK_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(h->pos) + n_fwd > h->cfg.max_seq) return MK_ERR_KV_FULL;
   if (cudaSetDevice(h->device) != cudaSuccess) return MK_ERR_CUDA;
 
   mk::Params p = h->base;
@@ -628,9 +629,10 @@ int mk_mailbox_read(mk_handle *h, int32_t *dst, int32_t cap, int32_t *n_out) {
 
 int mk_decode_host(mk_handle *h, const int32_t *h_in_ids, int32_t n_in, int32_t n_steps, int32_t *h_out_ids,
                    const mk_decode_opts *opts, mk_stream stream) {
-  if (!h || n_in < 0 || n_steps < 0 || !h_out_ids || (n_in > 0 && !h_in_ids)) return MK_ERR_INVALID_ARG;
+  if (!h || h->pending || n_in < 0 || n_steps < 0 || !h_out_ids || (n_in > 0 && !h_in_ids))
+    return MK_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(h->pos) + n_in + n_steps > h->cfg.max_seq) return MK_ERR_KV_FULL;
   const int n_fwd = n_in + n_steps;
-  if (n_fwd > h->cfg.max_seq) return MK_ERR_KV_FULL;
   if (n_fwd == 0) return MK_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaSetDevice(h->device) != cudaSuccess) return MK_ERR_CUDA;

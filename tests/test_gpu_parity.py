@@ -270,5 +270,19 @@ def test_errors_are_reported_not_raised_as_faults():
         dec.decode([1, 2], 1, spin_ns=20_000_000, fault_skip_barrier=1)
     assert e.value.code == -5
     dec.reset()
+    # forward counts whose sum does not fit an int32 are rejected before any
+    # launch (KV full) and leave the cursor where it was
+    import ctypes as C
+    d_in = torch.tensor([1], dtype=torch.int32, device="cuda:0")
+    d_out = torch.empty(8, dtype=torch.int32, device="cuda:0")
+    st = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    big = 2 ** 31 - 1
+    assert dec.lib.mk_decode(dec.h, C.c_void_p(d_in.data_ptr()), 1, big, C.c_void_p(d_out.data_ptr()),
+                             None, st) == -3
+    h_in = np.array([1], dtype=np.int32)
+    h_out = np.empty(8, dtype=np.int32)
+    assert dec.lib.mk_decode_host(dec.h, h_in.ctypes.data_as(C.c_void_p), 1, big,
+                                  h_out.ctypes.data_as(C.c_void_p), None, st) == -3
+    assert dec.info()["position"] == 0
     ids = dec.decode([1, 2], 2)                                   # the handle still works
     assert ids.shape[0] == 4
