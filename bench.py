@@ -498,6 +498,26 @@ def prefill_case(args):
         print("prefill case %d: %s, %d-token prompt, %.3f ms" % (rep, args.workload, n, e0.elapsed_time(e1)))
 
 
+def trace_case(args):
+    """Phase times of the decode kernel from its %globaltimer stamps: the
+    workload's prompt through ``mk_prefill``, then 64 traced greedy forwards."""
+    import torch
+    import persistent_transformer_megakernel_gb300 as mk
+    from persistent_transformer_megakernel_gb300 import trace as T
+    wl, s, desc = workload_desc(args.workload)
+    if wl.get("sentinel"):
+        raise SystemExit("--trace-case needs a workload with an id prompt")
+    w = W.make_weights(s, seed=0)
+    n = 64
+    dec = mk.Decoder(s, w, max_seq=wl["prompt"] + n + 8)
+    dec.prefill(W.make_prompt(s["vocab_in"], wl["prompt"], seed=1), all_ids=False)
+    buf = T.buffer(dec, n)
+    dec.decode(None, n, trace=buf)
+    torch.cuda.synchronize()
+    print("trace case: %s; %d greedy forwards after the prompt" % (desc, n))
+    print(T.format_summary(T.summarize(buf, s["n_layers"])))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -511,6 +531,8 @@ def main():
     ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--prefill-case", action="store_true",
                     help="run the workload's prompt through mk_prefill twice (the prefill ncu launch list)")
+    ap.add_argument("--trace-case", action="store_true",
+                    help="print the decode kernel's per-phase times from its in-kernel stamps")
     ap.add_argument("--ncu-case", action="store_true",
                     help="run only the small profiling case (no JSON line)")
     args = ap.parse_args()
@@ -519,6 +541,9 @@ def main():
         return
     if args.ncu_case:
         ncu_case(args)
+        return
+    if args.trace_case:
+        trace_case(args)
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -248,6 +248,24 @@ def test_host_buffer_entry_point_matches_device_one():
     assert np.array_equal(ia, ib)
 
 
+def test_phase_trace_stamps_are_ordered_and_change_nothing():
+    from persistent_transformer_megakernel_gb300 import trace as T
+    s = W.shape("mid")
+    w = W.make_weights(s, seed=0)
+    dec = mk.Decoder(s, w, max_seq=32)
+    ref = dec.decode([1, 2, 3], 3).cpu().numpy()
+    dec.reset()
+    buf = T.buffer(dec, 6)
+    ids = dec.decode([1, 2, 3], 3, trace=buf).cpu().numpy()
+    torch.cuda.synchronize()
+    assert np.array_equal(ids, ref)                       # the stamps change no result
+    summ = T.summarize(buf, s["n_layers"])                # raises on a missing or unordered stamp
+    assert all(summ["kinds"][k]["in_phase_us"] > 0 for k in T.KINDS)
+    assert len(summ["forward_us"]) == 6 and min(summ["forward_us"]) > 0
+    t = buf.cpu().numpy().reshape(-1, dec.info()["grid"], 4)
+    assert (t[1:, :, 0] >= t[:-1, :, 3]).all()            # every CTA takes the phases in order
+
+
 def test_errors_are_reported_not_raised_as_faults():
     s = W.shape("tiny")
     w = W.make_weights(s, seed=0)
