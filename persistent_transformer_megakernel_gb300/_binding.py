@@ -130,6 +130,50 @@ def _stream_ptr(stream) -> C.c_void_p:
     return C.c_void_p(s.cuda_stream)
 
 
+def check_options(shape: dict, n: int, *, out=None, embeds=None, pos3=None, logits=None, hidden=None,
+                  trace=None, grid: int = 0, talker=None, on_device: bool = True) -> None:
+    """Validate the tensors of an ``n``-forward call against what the kernel
+    reads and writes (the C ABI takes plain pointers and cannot check sizes):
+    ``out`` int32 >= n ids; ``logits`` fp32 >= n x vocab; ``hidden`` fp32 >=
+    n x (L + 1) x H; ``pos3`` int32 exactly 3 x n (three streams, row stride n);
+    ``embeds`` fp32 [rows][H]; ``trace`` int64 >= n x (5 L + 1) x grid x 4;
+    ``talker`` = (books bf16 [n_books][rows][H], text bf16 [rows][H], codes
+    int32 [code_rows][n_books], text_ids int32 [code_rows]).  Every tensor must
+    be contiguous (and on the device unless ``on_device`` is False).  Raises
+    ValueError."""
+    L, H, V = shape["n_layers"], shape["hidden"], shape["vocab"]
+
+    def need(t, name, dtype, numel=None, exact=False, dims=None):
+        if t is None:
+            return
+        if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_contiguous() or \
+                (on_device and not t.is_cuda):
+            raise ValueError("%s must be a contiguous device tensor of dtype %s" % (name, dtype))
+        if dims is not None and t.dim() != dims:
+            raise ValueError("%s must have %d dimensions" % (name, dims))
+        if numel is not None and (t.numel() != numel if exact else t.numel() < numel):
+            raise ValueError("%s holds %d elements; the call needs %s%d" %
+                             (name, t.numel(), "" if exact else "at least ", numel))
+
+    need(out, "out", torch.int32, n)
+    need(logits, "logits", torch.float32, n * V)
+    need(hidden, "hidden", torch.float32, n * (L + 1) * H)
+    need(pos3, "pos3", torch.int32, 3 * n, exact=True)
+    need(embeds, "embeds", torch.float32, dims=2)
+    if embeds is not None and embeds.shape[1] != H:
+        raise ValueError("embeds rows must have hidden (%d) elements" % H)
+    if trace is not None:
+        need(trace, "trace", torch.int64, n * (5 * L + 1) * grid * 4)
+    if talker is not None:
+        books, text, codes, text_ids = talker
+        need(books, "talker books", torch.bfloat16, dims=3)
+        need(text, "talker text", torch.bfloat16, dims=2)
+        need(codes, "talker codes", torch.int32, dims=2)
+        need(text_ids, "talker text_ids", torch.int32, codes.shape[0], exact=True)
+        if books.shape[2] != H or text.shape[1] != H or codes.shape[1] != books.shape[0]:
+            raise ValueError("talker tables must be [n_books][rows][H] and [rows][H], codes [rows][n_books]")
+
+
 def _dev_bf16(bits: np.ndarray, device) -> torch.Tensor:
     t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
     return t.to(device, non_blocking=False).contiguous()
@@ -266,16 +310,8 @@ class Decoder:
         n = n_in + n_steps
         if out is None:
             out = torch.empty(max(n, 1), dtype=torch.int32, device=self.device)
-        for t, dt in ((embeds, torch.float32), (logits, torch.float32), (hidden, torch.float32),
-                      (pos3, torch.int32)):
-            if t is not None and (t.dtype != dt or not t.is_cuda or not t.is_contiguous()):
-                raise ValueError("option tensors must be contiguous device tensors of the right dtype")
-        if talker is not None:
-            books, text, codes, text_ids = talker
-            if books.dtype != torch.bfloat16 or text.dtype != torch.bfloat16 or \
-                    codes.dtype != torch.int32 or text_ids.dtype != torch.int32 or \
-                    not all(t.is_cuda and t.is_contiguous() for t in talker):
-                raise ValueError("talker tables must be contiguous bf16 and ids contiguous int32 device tensors")
+        check_options(self.shape, n, out=out, embeds=embeds, pos3=pos3, logits=logits, hidden=hidden,
+                      trace=trace, grid=self.info()["grid"] if trace is not None else 0, talker=talker)
         o = self._opts(per_op, embeds, pos3, logits, hidden, trace, attn_chunks, spin_ns,
                        fault_skip_barrier, talker)
         rc = self.lib.mk_decode(self.h, _ptr(d_in), n_in, n_steps, _ptr(out), C.byref(o),
@@ -297,6 +333,8 @@ class Decoder:
         n = d_in.numel()
         if all_ids and out is None:
             out = torch.empty(max(n, 1), dtype=torch.int32, device=self.device)
+        check_options(self.shape, n, out=out if all_ids else None, embeds=embeds, pos3=pos3, logits=logits,
+                      hidden=hidden)
         o = self._opts(False, embeds, pos3, logits, hidden, None, 0, 0, -1)
         _check(self.lib.mk_prefill(self.h, _ptr(d_in), n, _ptr(out) if all_ids else None, C.byref(o),
                                    _stream_ptr(stream)), "mk_prefill")
@@ -319,6 +357,7 @@ class Decoder:
         n = n_in + n_steps
         if out is None:
             out = torch.empty(max(n, 1), dtype=torch.int32, device=self.device)
+        check_options(self.shape, n, out=out, embeds=embeds, pos3=pos3)
         o = self._opts(per_op, embeds, pos3, None, None, None, 0, 0, -1)
         if stream_ids:
             o.flags |= MK_DECODE_STREAM
@@ -373,6 +412,7 @@ class Decoder:
         ids = np.ascontiguousarray(np.asarray(in_ids, dtype=np.int32))
         n = ids.size + n_steps
         out = np.empty(max(n, 1), dtype=np.int32)
+        check_options(self.shape, n, embeds=embeds, pos3=pos3)
         o = self._opts(per_op, embeds, pos3, None, None, None, 0, 0, -1)
         rc = self.lib.mk_decode_host(self.h, ids.ctypes.data_as(C.c_void_p) if ids.size else None,
                                      ids.size, n_steps, out.ctypes.data_as(C.c_void_p), C.byref(o),
