@@ -1,0 +1,238 @@
+// Tensor-core GEMM of the batched prompt prefill (interface in mk_gemm.h).
+//
+// One CTA computes a 128 x BN tile of out^T (128 weight rows n, BN tokens t)
+// over its share of K, with three warp roles:
+//   warp 0     one lane issues the TMA loads of every K block (64 wide): the
+//              weight tile [128 x 64] and the three activation-term tiles
+//              [BN x 64], into a STAGES-deep shared-memory ring;
+//   warp 1     allocates the tensor-memory accumulator (128 lanes x BN fp32
+//              columns); one lane issues per K block 3 terms x 4 steps of
+//              tcgen05.mma (M 128, N BN, K 16), all into the one accumulator,
+//              and commits each stage back to the producer;
+//   warps 2-5  wait for the last commit, read the accumulator with
+//              tcgen05.ld (warp w owns TMEM lanes 32 (w % 4) ..) and store
+//              fp32 results, consecutive lanes writing consecutive n.
+// Every wait is bounded (2 s); on expiry the CTA records MK_ERR_TIMEOUT,
+// still waits for the MMAs it issued, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/mk.h"
+#include "mk_gemm.h"
+#include "mk_tc.cuh"
+
+namespace mkg {
+
+using namespace mktc;
+
+constexpr int GEMM_THREADS = 192;
+constexpr uint32_t A_BYTES = 128 * 128;    // weight tile: 128 rows x 64 bf16
+constexpr long long WAIT_NS = 2000000000LL;
+
+template <int BN, int STAGES>
+constexpr size_t gemm_smem() {
+  return 2048 + static_cast<size_t>(STAGES) * (A_BYTES + 3 * BN * 128);
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    pf_gemm(const __grid_constant__ WMaps wm, const __grid_constant__ CUtensorMap tx, const GemmCall c) {
+  constexpr uint32_t B_BYTES = BN * 128;                 // one activation term: BN rows x 64 bf16
+  constexpr uint32_t STAGE = A_BYTES + 3 * B_BYTES;
+  constexpr uint32_t TCOLS = BN < 32 ? 32 : BN;          // tensor-memory columns (a power of two)
+  constexpr uint32_t IDESC = idesc_bf16_f32(128, BN);
+  extern __shared__ unsigned char smraw[];
+  // 1024-byte alignment for the swizzled tiles
+  unsigned char *sm = smraw + ((1024u - (smem_addr(smraw) & 1023u)) & 1023u);
+  uint64_t *full = reinterpret_cast<uint64_t *>(sm);
+  uint64_t *empty = full + STAGES;
+  uint64_t *accum = empty + STAGES;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(accum + 1);
+  unsigned char *ring = sm + 1024;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * BN, sp = blockIdx.z;
+  // the weight matrix of this row tile, its first row, and the output column of that row
+  int mi = 0, tile = blockIdx.y, col0 = 0;
+  while (mi + 1 < wm.n && tile >= (wm.rows[mi] + 127) / 128) {
+    tile -= (wm.rows[mi] + 127) / 128;
+    col0 += wm.rows[mi];
+    ++mi;
+  }
+  const int n0 = tile * 128, nrows = wm.rows[mi];
+  const CUtensorMap *tw = &wm.map[mi];
+  const int KB = c.K / 64;
+  const int per = (KB + c.splits - 1) / c.splits;
+  const int kb0 = sp * per;
+  const int nk = max(0, min(KB, kb0 + per) - kb0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum, 1);
+    fence_mbar_init();
+    prefetch_tmap(tw);
+    prefetch_tmap(&tx);
+  }
+  if (warp == 1) tmem_alloc(tslot, TCOLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // the activation terms are re-read by every weight tile: keep them in L2
+      const uint64_t keep = l2_evict_last();
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % STAGES;
+        if (i >= STAGES && !mbar_wait(&empty[s], ((i / STAGES) - 1) & 1, WAIT_NS)) {
+          atomicCAS(c.err, 0, MK_ERR_TIMEOUT);
+          break;
+        }
+        unsigned char *st = ring + s * STAGE;
+        mbar_expect_tx(&full[s], STAGE);
+        const int kx = (kb0 + i) * 64;
+        tma_load_2d(st, tw, kx, n0, &full[s]);
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+          tma_load_3d_hint(st + A_BYTES + j * B_BYTES, &tx, kx, c.t_off + t0, j, &full[s], keep);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int i = 0; i < nk; ++i) {
+        const int s = i % STAGES;
+        if (!mbar_wait(&full[s], (i / STAGES) & 1, WAIT_NS)) {
+          atomicCAS(c.err, 0, MK_ERR_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_addr(ring + s * STAGE);
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16(tbase, desc_sw128(sa + 32 * k), desc_sw128(sa + A_BYTES + j * B_BYTES + 32 * k), IDESC,
+                     (i | j | k) != 0);
+        mma_commit(&empty[s]);
+      }
+      // completes once every MMA issued above has finished (on the error path too)
+      mma_commit(accum);
+    }
+  } else {
+    const int q = warp & 3;                              // the TMEM lane quarter this warp may read
+    const bool ok = mbar_wait(accum, 0, WAIT_NS);
+    tc_fence_after();
+    if (!ok) {
+      if (lane == 0) atomicCAS(c.err, 0, MK_ERR_TIMEOUT);
+    } else if (nk > 0) {
+      const int r = n0 + 32 * q + lane;                  // row of this matrix
+      float *o = c.out + static_cast<size_t>(sp) * c.part_stride + col0;
+#pragma unroll 1
+      for (int cc = 0; cc < BN; cc += 16) {
+        if (t0 + cc >= c.nt) break;                      // warp-uniform
+        float v[16];
+        tmem_ld16(tbase + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(cc), v);
+        if (r < nrows) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (t0 + cc + i < c.nt) o[static_cast<size_t>(t0 + cc + i) * c.ldc + r] = v[i];
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tbase, TCOLS);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    cudaDriverEntryPointQueryResult q;
+    void *p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+template <int BN, int STAGES>
+int launch(const WMaps &w, const CUtensorMap &x, const GemmCall &c, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(pf_gemm<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(gemm_smem<BN, STAGES>())) != cudaSuccess) {
+      cudaGetLastError();
+      return MK_ERR_CUDA;
+    }
+    attr = true;
+  }
+  int tiles = 0;
+  for (int i = 0; i < w.n; ++i) tiles += (w.rows[i] + 127) / 128;
+  const dim3 grid((c.nt + BN - 1) / BN, tiles, c.splits);
+  pf_gemm<BN, STAGES><<<grid, GEMM_THREADS, gemm_smem<BN, STAGES>(), s>>>(w, x, c);
+  return cudaGetLastError() == cudaSuccess ? MK_OK : MK_ERR_CUDA;
+}
+
+}  // namespace
+
+bool make_tmap(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+               uint32_t box_rows, uint64_t planes, uint64_t plane_bytes) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc || (reinterpret_cast<uintptr_t>(base) & 15u) || (row_bytes & 15u) || inner % 64 || box_rows == 0 ||
+      box_rows > 256 || planes < 1 || (planes > 1 && (plane_bytes & 15u)))
+    return false;
+  const cuuint64_t dims[3] = {inner, outer, planes};
+  const cuuint64_t strides[2] = {row_bytes, plane_bytes};
+  const cuuint32_t box[3] = {64, box_rows, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, planes > 1 ? 3 : 2, const_cast<void *>(base), dims, strides, box,
+             es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int gemm_block_tokens(int nt) { return nt <= 32 ? 32 : nt <= 64 ? 64 : 128; }
+
+int gemm_splits(int N, int K, int nt, int sms, int max_splits) {
+  const int KB = K / 64;
+  const long long tiles = static_cast<long long>((nt + gemm_block_tokens(nt) - 1) / gemm_block_tokens(nt)) *
+                          ((N + 127) / 128);
+  int s = 1;
+  while (2 * s <= max_splits && KB % (2 * s) == 0 && KB / (2 * s) >= 4 && tiles * s < sms) s *= 2;
+  return s;
+}
+
+int gemm_launch(const WMaps &w, const CUtensorMap &x, const GemmCall &c, cudaStream_t s) {
+  int rows = 0;
+  for (int i = 0; i < w.n && i < 3; ++i) rows += w.rows[i] > 0 ? w.rows[i] : -(1 << 30);
+  if (w.n < 1 || w.n > 3 || rows != c.N) return MK_ERR_INVALID_ARG;
+  if (c.N < 1 || c.K < 64 || c.K % 64 || c.nt < 1 || c.t_off < 0 || c.splits < 1 || (c.K / 64) % c.splits || !c.out || !c.err ||
+      c.ldc < static_cast<size_t>(c.N))
+    return MK_ERR_INVALID_ARG;
+  switch (gemm_block_tokens(c.nt)) {
+    case 32: return launch<32, 4>(w, x, c, s);
+    case 64: return launch<64, 4>(w, x, c, s);
+    default: return launch<128, 3>(w, x, c, s);
+  }
+}
+
+}  // namespace mkg

@@ -1,9 +1,10 @@
 // Batched prompt prefill: the n prompt forwards of a decode call computed all
 // at once per layer.  The projections are dense contractions with M = prompt
-// tokens and run as bf16 tensor-core GEMMs with fp32 accumulation (cuBLAS);
-// every fp32 activation enters them as three bf16 terms (hi + mid + lo, 24
-// significant bits, as many as fp32 holds), so the products lose nothing to
-// the bf16 operand format.  The
+// tokens and run on the tensor cores (csrc/mk_gemm.cu: tcgen05.mma, bf16
+// operands staged by TMA, fp32 accumulators in tensor memory); every fp32
+// activation enters them as three bf16 terms (hi + mid + lo, 24 significant
+// bits, as many as fp32 holds) accumulated into one fp32 sum, so the products
+// lose nothing to the bf16 operand format.  The
 // rest -- RMSNorm, QK-norm, RoPE / MRoPE, the bf16 KV append, causal GQA
 // attention over the cache, residual adds, SiLU * up, greedy argmax -- are the
 // kernels below.  The KV cache it fills is the decode kernel's, so decoding
@@ -11,13 +12,12 @@
 // persistent CUDA megakernel to Qwen3-TTS": time to first chunk is what the
 // listener waits for).
 #include <cuda_runtime.h>
-#include <cublas_v2.h>
-#include <cuda_bf16.h>
 
 #include <cmath>
 #include <cstdint>
 #include <cstring>
 
+#include "mk_gemm.h"
 #include "mk_prefill.h"
 
 namespace mkp {
@@ -42,9 +42,11 @@ __device__ __forceinline__ void split3(float v, uint16_t &hi, uint16_t &mid, uin
   lo = f2bf(r1 - bf2f(mid));
 }
 
-// a GEMM output element: the sum of its three partials (one per input term)
-__device__ __forceinline__ float sum3(const float *c, size_t stride, size_t i) {
-  return (c[i] + c[stride + i]) + c[2 * stride + i];
+// a GEMM output element: the sum of its split-K partials (stride apart), in split order
+__device__ __forceinline__ float sum_parts(const float *c, size_t stride, int n, size_t i) {
+  float v = c[i];
+  for (int s = 1; s < n; ++s) v += c[s * stride + i];
+  return v;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -89,9 +91,9 @@ __global__ void pf_embed(const PfArgs a, int t0, int nt) {
 
 // Optionally x[t] += y[t] (a residual add) and record hidden[t][layer]; then
 // h = x / sqrt(mean(x^2) + eps) * gain as three bf16 terms
-__global__ void pf_add_norm_split(const PfArgs a, const float *y, const uint16_t *gain, int t0, int nt,
+__global__ void pf_add_norm_split(const PfArgs a, const float *y, int ny, const uint16_t *gain, int t0, int nt,
                                   int hidden_layer) {
-  // y: three partials of the GEMM output, a.y_stride apart, or NULL
+  // y: ny split-K partials of the GEMM output, a.y_stride apart, or NULL
   __shared__ float red[PF_THREADS / 32];
   const int t = blockIdx.x;
   if (t >= nt) return;
@@ -100,7 +102,7 @@ __global__ void pf_add_norm_split(const PfArgs a, const float *y, const uint16_t
   for (int k = threadIdx.x; k < a.H; k += blockDim.x) {
     float v = x[k];
     if (y) {
-      v = v + sum3(y, a.y_stride, static_cast<size_t>(t) * a.H + k);
+      v = v + sum_parts(y, a.y_stride, ny, static_cast<size_t>(t) * a.H + k);
       x[k] = v;
       if (a.call->hidden && hidden_layer >= 0)
         a.call->hidden[(static_cast<size_t>(t0 + t) * (a.L + 1) + hidden_layer) * a.H + k] = v;
@@ -124,14 +126,18 @@ __global__ void pf_split(const float *v, int n, int nt, uint16_t *hs, size_t hs_
     split3(v[i], hs[i], hs[hs_stride + i], hs[2 * hs_stride + i]);
 }
 
-// u = silu(gate) * up from the GEMM partials (c_stride apart), as three bf16 terms
-__global__ void pf_silu_mul_split(const float *g, const float *u, size_t c_stride, int n, int nt, uint16_t *hs,
+// u = silu(gate) * up from the GEMM partials (nc of them, c_stride apart; row t
+// holds the n gate columns, then the n up columns), as three bf16 terms
+__global__ void pf_silu_mul_split(const float *gu, size_t c_stride, int nc, int n, int nt, uint16_t *hs,
                                   size_t hs_stride) {
   const size_t total = static_cast<size_t>(n) * nt;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const float z = sum3(g, c_stride, i);
-    split3(z / (1.0f + expf(-z)) * sum3(u, c_stride, i), hs[i], hs[hs_stride + i], hs[2 * hs_stride + i]);
+    const size_t t = i / n, c = i - t * n;
+    const size_t gi = t * 2 * n + c;
+    const float z = sum_parts(gu, c_stride, nc, gi);
+    split3(z / (1.0f + expf(-z)) * sum_parts(gu, c_stride, nc, gi + n), hs[i], hs[hs_stride + i],
+           hs[2 * hs_stride + i]);
   }
 }
 
@@ -164,7 +170,7 @@ __global__ void pf_qk_rope_append(const PfArgs a, int layer, const uint16_t *q_n
   const size_t base = static_cast<size_t>(t) * rows + static_cast<size_t>(job) * HD;
   float v[EPL];
 #pragma unroll
-  for (int k = 0; k < EPL; ++k) v[k] = sum3(a.qkv3, a.qkv_stride, base + lane + 32 * k);
+  for (int k = 0; k < EPL; ++k) v[k] = sum_parts(a.qkv_p, a.qkv_stride, a.qkv_n, base + lane + 32 * k);
   if (job < a.Hq + a.Hkv) {
     const uint16_t *gain = job < a.Hq ? q_norm : k_norm;
     float ss = 0.f;
@@ -422,17 +428,17 @@ __global__ void __launch_bounds__(PF_THREADS) pf_attention(const PfArgs a, int l
   }
 }
 
-// Greedy id of each token, in two stages: block (t, b) sums the three logit
-// partials of its slice of the vocabulary (storing them in logits_out when
-// given) and keeps its best (largest value, lowest index among equals); then
+// Greedy id of each token, in two stages: block (t, b) reads the logits of
+// its slice of the vocabulary (storing them in logits_out when given) and
+// keeps its best (largest value, lowest index among equals); then
 // one warp per token reduces the blocks' candidates.  A non-finite logit is
 // an error.
 constexpr int PF_ARGMAX_BLOCKS = 64;
 
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
-__global__ void pf_argmax_part(const float *lg3, size_t stride, int V, int t_first, const PfCall *call, float *pv,
-                               int *pi, int *err) {
+__global__ void pf_argmax_part(const float *lg, int V, int t_first, const PfCall *call, float *pv, int *pi,
+                               int *err) {
   float *logits_out = call->logits_out;
   __shared__ float sv[PF_THREADS / 32];
   __shared__ int si[PF_THREADS / 32];
@@ -442,7 +448,7 @@ __global__ void pf_argmax_part(const float *lg3, size_t stride, int V, int t_fir
   float v = -INFINITY;
   int i = 0x7fffffff;
   for (int k = k0 + threadIdx.x; k < k1; k += blockDim.x) {
-    const float y = sum3(lg3, stride, static_cast<size_t>(t) * V + k);
+    const float y = lg[static_cast<size_t>(t) * V + k];
     if (logits_out) logits_out[static_cast<size_t>(t_first + t) * V + k] = y;
     if (!isfinite(y)) atomicCAS(err, 0, MK_PF_ERR_NUMERIC);
     if (better(y, k, v, i)) { v = y; i = k; }
@@ -495,8 +501,6 @@ __global__ void pf_argmax_final(const float *pv, const int *pi, int t_first, con
 namespace mkp {
 namespace {
 
-constexpr size_t kBlasWorkspace = 32u << 20;   // bytes
-
 template <typename T>
 int dalloc(T **p, size_t n) {
   if (cudaMalloc(reinterpret_cast<void **>(p), sizeof(T) * (n ? n : 1)) != cudaSuccess) {
@@ -507,20 +511,25 @@ int dalloc(T **p, size_t n) {
   return MK_OK;
 }
 
-// C_i[nt][N] (ldc) = term_i[nt][K] . W[N][K]^T for the three bf16 terms of the
-// input (term i at in + i * in_stride, C_i at C + i * c_stride), fp32 accumulate
-// on tensor cores, one batched call; the readers add C_0 + C_1 + C_2.  In
-// column-major terms C_i^T (N x nt) = W (N x K, stored as K x N) . term_i^T.
-int gemm3(cublasHandle_t b, const uint16_t *in, long long in_stride, const uint16_t *W, int nt, int N, int K,
-          float *C, int ldc, long long c_stride) {
-  const float one = 1.0f, zero = 0.0f;
-  const cublasStatus_t st = cublasGemmStridedBatchedEx(
-      b, CUBLAS_OP_T, CUBLAS_OP_N, N, nt, K, &one, W, CUDA_R_16BF, K, 0, in, CUDA_R_16BF, K, in_stride, &zero, C,
-      CUDA_R_32F, ldc, c_stride, 3, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-  return st == CUBLAS_STATUS_SUCCESS ? MK_OK : MK_ERR_CUDA;
-}
-
 int blocks_for(size_t n) { return static_cast<int>((n + PF_THREADS - 1) / PF_THREADS > 4096 ? 4096 : (n + PF_THREADS - 1) / PF_THREADS); }
+
+int block_index(int bn) { return bn == 32 ? 0 : bn == 64 ? 1 : 2; }
+
+// one projection: out[s][t][n] (n < N, t < nt) = W[n][:] . (three terms of token t_off + t)
+int project(const PfState &st, const mkg::WMaps &w, int kidx, int N, int K, int nt, int t_off, int splits,
+            float *out, size_t ldc, size_t part_stride, cudaStream_t s) {
+  mkg::GemmCall c;
+  c.N = N;
+  c.K = K;
+  c.nt = nt;
+  c.t_off = t_off;
+  c.splits = splits;
+  c.out = out;
+  c.ldc = ldc;
+  c.part_stride = part_stride;
+  c.err = st.err;
+  return mkg::gemm_launch(w, st.xmaps[kidx][block_index(mkg::gemm_block_tokens(nt))], c, s);
+}
 
 }  // namespace
 
@@ -546,33 +555,49 @@ bool pf_attention_enable() {
 int pf_init(PfState &st, int tc, int H, int Hq, int Hkv, int d, int I) {
   if (st.tc >= tc) return MK_OK;
   pf_free(st);
+  if (H % 64 || (Hq * d) % 64 || I % 64) return MK_ERR_UNSUPPORTED;   // GEMM K blocks of 64
   const size_t rows = static_cast<size_t>(Hq + 2 * Hkv) * d;
   size_t kmax = H;
   if (static_cast<size_t>(Hq) * d > kmax) kmax = static_cast<size_t>(Hq) * d;
   if (static_cast<size_t>(I) > kmax) kmax = I;
-  cublasHandle_t b = nullptr;
-  if (cublasCreate(&b) != CUBLAS_STATUS_SUCCESS) return MK_ERR_CUDA;
-  st.blas = b;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MK_ERR_CUDA;
+  }
   const size_t T = tc;
   int rc;
   if ((rc = dalloc(&st.x, T * H)) || (rc = dalloc(&st.qkv, T * rows)) || (rc = dalloc(&st.attn, T * Hq * d)) ||
-      (rc = dalloc(&st.qkv3, 3 * T * rows)) || (rc = dalloc(&st.y3, 3 * T * H)) ||
-      (rc = dalloc(&st.gate3, 3 * T * I)) || (rc = dalloc(&st.up3, 3 * T * I)) ||
+      (rc = dalloc(&st.qkv_p, PF_SPLITS_WIDE * T * rows)) || (rc = dalloc(&st.y_p, PF_SPLITS_NARROW * T * H)) ||
+      (rc = dalloc(&st.gu_p, PF_SPLITS_WIDE * T * 2 * I)) ||
       (rc = dalloc(&st.hs, 3 * T * kmax)) || (rc = dalloc(&st.pv, T * PF_ARGMAX_BLOCKS)) ||
-      (rc = dalloc(&st.pi, T * PF_ARGMAX_BLOCKS)) || (rc = dalloc(&st.err, 1)) || (rc = dalloc(&st.call, 1)) ||
-      (rc = dalloc(reinterpret_cast<unsigned char **>(&st.blas_ws), kBlasWorkspace))) {
+      (rc = dalloc(&st.pi, T * PF_ARGMAX_BLOCKS)) || (rc = dalloc(&st.err, 1)) || (rc = dalloc(&st.call, 1))) {
     pf_free(st);
     return rc;
   }
-  // a fixed workspace: the library then allocates nothing while a prefill is captured
-  if (cublasSetWorkspace(b, st.blas_ws, kBlasWorkspace) != CUBLAS_STATUS_SUCCESS ||
+  st.tc = tc;
+  st.kmax = kmax;
+  // the input terms of tokens past a chunk's end are read (never stored): keep them finite
+  if (cudaMemset(st.hs, 0, sizeof(uint16_t) * 3 * T * kmax) != cudaSuccess ||
       cudaStreamCreateWithFlags(&st.cap, cudaStreamNonBlocking) != cudaSuccess || !pf_attention_enable()) {
     cudaGetLastError();
     pf_free(st);
     return MK_ERR_CUDA;
   }
-  st.tc = tc;
-  st.kmax = kmax;
+  // activation tensor maps: the three term matrices [tc][K] (rows K apart, as
+  // the split kernels write them for a GEMM of input width K), T * kmax apart
+  const int Ks[3] = {H, Hq * d, I};
+  const int bns[3] = {32, 64, 128};
+  for (int i = 0; i < 3; ++i)
+    for (int b = 0; b < 3; ++b) {
+      std::memset(&st.xmaps[i][b], 0, sizeof(CUtensorMap));
+      if (!mkg::make_tmap(&st.xmaps[i][b], st.hs, Ks[i], T, static_cast<uint64_t>(Ks[i]) * 2, bns[b], 3,
+                          T * kmax * 2)) {
+        pf_free(st);
+        return MK_ERR_CUDA;
+      }
+    }
   return MK_OK;
 }
 
@@ -582,67 +607,65 @@ void pf_free(PfState &st) {
     cudaGraphDestroy(g.graph);
   }
   if (st.cap) cudaStreamDestroy(st.cap);
-  void *ps[] = {st.x,  st.qkv, st.attn, st.qkv3, st.y3, st.gate3,   st.up3,
-                st.logits3, st.pv, st.pi, st.hs, st.err, st.call, st.blas_ws};
+  void *ps[] = {st.x, st.qkv, st.attn, st.qkv_p, st.y_p, st.gu_p, st.logits, st.pv, st.pi, st.hs, st.err, st.call};
   for (void *p : ps)
     if (p) cudaFree(p);
-  if (st.blas) cublasDestroy(static_cast<cublasHandle_t>(st.blas));
   st = PfState();
 }
 
 // every launch of an n-token prefill, in order, on stream s
 int pf_enqueue(PfState &st, const PfArgs &a, const PfLayer *layers, const uint16_t *final_norm,
                const uint16_t *lm_head, int n, bool all_logits, cudaStream_t s) {
-  cublasHandle_t b = static_cast<cublasHandle_t>(st.blas);
-  if (cublasSetStream(b, s) != CUBLAS_STATUS_SUCCESS) return MK_ERR_CUDA;
+  (void)lm_head;
   const int rows = (a.Hq + 2 * a.Hkv) * a.d;
   const int grp = a.Hq / a.Hkv;
+  const int qd = a.Hq * a.d;
   const size_t T = st.tc;
-  const long long hs_s = static_cast<long long>(a.hs_stride);
-  const long long ffn_s = static_cast<long long>(T) * a.I, lg_s = static_cast<long long>(T) * a.V;
+  const size_t gu_stride = T * 2 * a.I;
   int rc = MK_OK;
   for (int t0 = 0; t0 < n && rc == MK_OK; t0 += st.tc) {
     const int nt = n - t0 < st.tc ? n - t0 : st.tc;
-    pf_embed<<<nt, PF_THREADS, 0, s>>>(a, t0, nt);
-    pf_add_norm_split<<<nt, PF_THREADS, 0, s>>>(a, nullptr, layers[0].attn_norm, t0, nt, -1);
+    // split-K counts of this chunk's projections (the readers sum that many partials)
+    const int s_qkv = mkg::gemm_splits(rows, a.H, nt, st.sms, PF_SPLITS_WIDE);
+    const int s_o = mkg::gemm_splits(a.H, qd, nt, st.sms, PF_SPLITS_NARROW);
+    const int s_gu = mkg::gemm_splits(2 * a.I, a.H, nt, st.sms, PF_SPLITS_WIDE);
+    const int s_dn = mkg::gemm_splits(a.H, a.I, nt, st.sms, PF_SPLITS_NARROW);
+    PfArgs ac = a;
+    ac.qkv_n = s_qkv;
+    pf_embed<<<nt, PF_THREADS, 0, s>>>(ac, t0, nt);
+    pf_add_norm_split<<<nt, PF_THREADS, 0, s>>>(ac, nullptr, 0, layers[0].attn_norm, t0, nt, -1);
     for (int l = 0; l < a.L && rc == MK_OK; ++l) {
       const PfLayer &w = layers[l];
-      // attention block
-      if ((rc = gemm3(b, st.hs, hs_s, w.wq, nt, a.Hq * a.d, a.H, st.qkv3, rows, a.qkv_stride)) ||
-          (rc = gemm3(b, st.hs, hs_s, w.wk, nt, a.Hkv * a.d, a.H, st.qkv3 + a.Hq * a.d, rows, a.qkv_stride)) ||
-          (rc = gemm3(b, st.hs, hs_s, w.wv, nt, a.Hkv * a.d, a.H, st.qkv3 + (a.Hq + a.Hkv) * a.d, rows,
-                      a.qkv_stride)))
-        break;
+      const mkg::WMaps *wm = &st.wmaps[static_cast<size_t>(l) * 4];
+      // attention block: q, k and v columns of one [nt][rows] output, s_qkv partials
+      if ((rc = project(st, wm[0], 0, rows, a.H, nt, 0, s_qkv, st.qkv_p, rows, a.qkv_stride, s))) break;
       const int jobs_warps = nt * (a.Hq + 2 * a.Hkv);
       const int wpb = PF_THREADS / 32;
       if (a.d == 64) {
-        pf_qk_rope_append<64><<<(jobs_warps + wpb - 1) / wpb, PF_THREADS, 0, s>>>(a, l, w.q_norm, w.k_norm, t0, nt);
+        pf_qk_rope_append<64><<<(jobs_warps + wpb - 1) / wpb, PF_THREADS, 0, s>>>(ac, l, w.q_norm, w.k_norm, t0, nt);
         // groups mk_create accepts: group * head_dim <= 256
         switch (grp) {
-          case 1: launch_attention<64, 1>(a, l, t0, nt, s); break;
-          case 2: launch_attention<64, 2>(a, l, t0, nt, s); break;
-          default: launch_attention<64, 4>(a, l, t0, nt, s); break;
+          case 1: launch_attention<64, 1>(ac, l, t0, nt, s); break;
+          case 2: launch_attention<64, 2>(ac, l, t0, nt, s); break;
+          default: launch_attention<64, 4>(ac, l, t0, nt, s); break;
         }
       } else {
-        pf_qk_rope_append<128><<<(jobs_warps + wpb - 1) / wpb, PF_THREADS, 0, s>>>(a, l, w.q_norm, w.k_norm, t0, nt);
+        pf_qk_rope_append<128><<<(jobs_warps + wpb - 1) / wpb, PF_THREADS, 0, s>>>(ac, l, w.q_norm, w.k_norm, t0, nt);
         switch (grp) {
-          case 1: launch_attention<128, 1>(a, l, t0, nt, s); break;
-          default: launch_attention<128, 2>(a, l, t0, nt, s); break;
+          case 1: launch_attention<128, 1>(ac, l, t0, nt, s); break;
+          default: launch_attention<128, 2>(ac, l, t0, nt, s); break;
         }
       }
-      pf_split<<<blocks_for(static_cast<size_t>(nt) * a.Hq * a.d), PF_THREADS, 0, s>>>(st.attn, a.Hq * a.d, nt,
-                                                                                         st.hs, a.hs_stride);
-      if ((rc = gemm3(b, st.hs, hs_s, w.wo, nt, a.H, a.Hq * a.d, st.y3, a.H, a.y_stride))) break;
-      pf_add_norm_split<<<nt, PF_THREADS, 0, s>>>(a, st.y3, w.mlp_norm, t0, nt, -1);
+      pf_split<<<blocks_for(static_cast<size_t>(nt) * qd), PF_THREADS, 0, s>>>(st.attn, qd, nt, st.hs, a.hs_stride);
+      if ((rc = project(st, wm[1], 1, a.H, qd, nt, 0, s_o, st.y_p, a.H, a.y_stride, s))) break;
+      pf_add_norm_split<<<nt, PF_THREADS, 0, s>>>(ac, st.y_p, s_o, w.mlp_norm, t0, nt, -1);
       // MLP block
-      if ((rc = gemm3(b, st.hs, hs_s, w.w_gate, nt, a.I, a.H, st.gate3, a.I, ffn_s)) ||
-          (rc = gemm3(b, st.hs, hs_s, w.w_up, nt, a.I, a.H, st.up3, a.I, ffn_s)))
-        break;
+      if ((rc = project(st, wm[2], 0, 2 * a.I, a.H, nt, 0, s_gu, st.gu_p, 2 * a.I, gu_stride, s))) break;
       pf_silu_mul_split<<<blocks_for(static_cast<size_t>(nt) * a.I), PF_THREADS, 0, s>>>(
-          st.gate3, st.up3, static_cast<size_t>(ffn_s), a.I, nt, st.hs, a.hs_stride);
-      if ((rc = gemm3(b, st.hs, hs_s, w.w_down, nt, a.H, a.I, st.y3, a.H, a.y_stride))) break;
-      pf_add_norm_split<<<nt, PF_THREADS, 0, s>>>(a, st.y3, l + 1 < a.L ? layers[l + 1].attn_norm : final_norm, t0,
-                                                   nt, l + 1);
+          st.gu_p, gu_stride, s_gu, a.I, nt, st.hs, a.hs_stride);
+      if ((rc = project(st, wm[3], 2, a.H, a.I, nt, 0, s_dn, st.y_p, a.H, a.y_stride, s))) break;
+      pf_add_norm_split<<<nt, PF_THREADS, 0, s>>>(ac, st.y_p, s_dn, l + 1 < a.L ? layers[l + 1].attn_norm : final_norm,
+                                                  t0, nt, l + 1);
     }
     if (rc != MK_OK) break;
     // LM head: every token of the chunk when ids or logits are wanted, else
@@ -650,10 +673,11 @@ int pf_enqueue(PfState &st, const PfArgs &a, const PfLayer *layers, const uint16
     const bool has_last = (t0 + nt == n);
     if (all_logits || has_last) {
       const int first = all_logits ? 0 : nt - 1, m = all_logits ? nt : 1;
-      const size_t off = static_cast<size_t>(first) * a.H;
-      if ((rc = gemm3(b, st.hs + off, hs_s, lm_head, m, a.V, a.H, st.logits3, a.V, lg_s))) break;
-      pf_argmax_part<<<dim3(PF_ARGMAX_BLOCKS, m), PF_THREADS, 0, s>>>(st.logits3, static_cast<size_t>(lg_s), a.V,
-                                                                     t0 + first, st.call, st.pv, st.pi, st.err);
+      if ((rc = project(st, st.wmaps[static_cast<size_t>(a.L) * 4], 0, a.V, a.H, m, first, 1, st.logits, a.V,
+                        0, s)))
+        break;
+      pf_argmax_part<<<dim3(PF_ARGMAX_BLOCKS, m), PF_THREADS, 0, s>>>(st.logits, a.V, t0 + first, st.call, st.pv,
+                                                                     st.pi, st.err);
       pf_argmax_final<<<m, 32, 0, s>>>(st.pv, st.pi, t0 + first, st.call, n - 1);
     }
   }
@@ -667,18 +691,46 @@ int pf_run(PfState &st, PfArgs a, const PfLayer *layers, const uint16_t *final_n
   if ((a.d != 64 && a.d != 128) || a.Hq % a.Hkv || (grp != 1 && grp != 2 && grp != 4 && !(grp == 8 && a.d == 64)))
     return MK_ERR_UNSUPPORTED;
   const size_t T = st.tc;
-  if (!st.logits3) {
-    int rc = dalloc(&st.logits3, 3 * T * a.V);
+  const bool all_logits = call.out_ids || call.logits_out;
+  const int need_rows = all_logits ? st.tc : 1;
+  if (st.logit_rows < need_rows) {
+    if (st.logits) cudaFree(st.logits);
+    st.logits = nullptr;
+    st.logit_rows = 0;
+    int rc = dalloc(&st.logits, static_cast<size_t>(need_rows) * a.V);
     if (rc) return rc;
+    st.logit_rows = need_rows;
+  }
+  if (st.wmaps.empty()) {
+    // weight tensor maps, made once per handle (the weights are borrowed for its lifetime)
+    std::vector<mkg::WMaps> m(static_cast<size_t>(a.L) * 4 + 1);
+    std::memset(m.data(), 0, sizeof(mkg::WMaps) * m.size());
+    const int qd = a.Hq * a.d, kd = a.Hkv * a.d;
+    // one stacked set of weight matrices per projection
+    auto set = [](mkg::WMaps &w, int i, const void *base, int K, int rows) {
+      w.rows[i] = rows;
+      w.n = i + 1;
+      return mkg::make_tmap(&w.map[i], base, K, rows, K * 2ull, 128);
+    };
+    bool ok = true;
+    for (int l = 0; l < a.L && ok; ++l) {
+      const PfLayer &w = layers[l];
+      mkg::WMaps *q = &m[static_cast<size_t>(l) * 4];
+      ok = set(q[0], 0, w.wq, a.H, qd) && set(q[0], 1, w.wk, a.H, kd) && set(q[0], 2, w.wv, a.H, kd) &&
+           set(q[1], 0, w.wo, qd, a.H) && set(q[2], 0, w.w_gate, a.H, a.I) && set(q[2], 1, w.w_up, a.H, a.I) &&
+           set(q[3], 0, w.w_down, a.I, a.H);
+    }
+    ok = ok && set(m[static_cast<size_t>(a.L) * 4], 0, lm_head, a.H, a.V);
+    if (!ok) return MK_ERR_CUDA;
+    st.wmaps.swap(m);
   }
   const int rows = (a.Hq + 2 * a.Hkv) * a.d;
   a.x = st.x; a.qkv = st.qkv; a.attn = st.attn;
-  a.qkv3 = st.qkv3; a.qkv_stride = T * rows;
-  a.y3 = st.y3; a.y_stride = T * a.H;
+  a.qkv_p = st.qkv_p; a.qkv_stride = T * rows;
+  a.y_p = st.y_p; a.y_stride = T * a.H;
   a.hs = st.hs; a.hs_stride = T * st.kmax;
   a.call = st.call;
   a.err = st.err;
-  const bool all_logits = call.out_ids || call.logits_out;
   // the call's fields, then the (captured once, replayed) launch sequence
   if (cudaMemcpyAsync(st.call, &call, sizeof(PfCall), cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemsetAsync(st.err, 0, sizeof(int), s) != cudaSuccess) {
@@ -686,8 +738,11 @@ int pf_run(PfState &st, PfArgs a, const PfLayer *layers, const uint16_t *final_n
     return MK_ERR_CUDA;
   }
   cudaGraphExec_t exec = nullptr;
-  for (const PfState::Graph &g : st.graphs)
-    if (g.n == n && g.all_logits == all_logits) exec = g.exec;
+  for (PfState::Graph &g : st.graphs)
+    if (g.n == n && g.all_logits == all_logits) {
+      exec = g.exec;
+      g.used = ++st.clock;
+    }
   int rc = MK_OK;
   if (!exec) {
     cudaGraph_t graph = nullptr;
@@ -699,7 +754,16 @@ int pf_run(PfState &st, PfArgs a, const PfLayer *layers, const uint16_t *final_n
       else e = e2 != cudaSuccess ? e2 : cudaErrorUnknown;
     }
     if (e == cudaSuccess && rc == MK_OK && exec) {
-      st.graphs.push_back(PfState::Graph{n, all_logits, graph, exec});
+      if (static_cast<int>(st.graphs.size()) >= PF_MAX_GRAPHS) {
+        // keep the cache bounded: replace the least recently used prompt length
+        size_t lru = 0;
+        for (size_t i = 1; i < st.graphs.size(); ++i)
+          if (st.graphs[i].used < st.graphs[lru].used) lru = i;
+        cudaGraphExecDestroy(st.graphs[lru].exec);
+        cudaGraphDestroy(st.graphs[lru].graph);
+        st.graphs.erase(st.graphs.begin() + static_cast<long>(lru));
+      }
+      st.graphs.push_back(PfState::Graph{n, all_logits, ++st.clock, graph, exec});
     } else {
       // not capturable here: run the same sequence directly
       if (graph) cudaGraphDestroy(graph);

@@ -1,12 +1,14 @@
 // Batched prompt prefill (csrc/mk_prefill.cu): interface between the C ABI in
-// mk_host.cu and the prefill kernels + tensor-core GEMMs.
+// mk_host.cu and the prefill kernels + tensor-core GEMMs (csrc/mk_gemm.cu).
 #pragma once
 #include <cstdint>
 #include <cstddef>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <vector>
 
 #include "../../include/mk.h"
+#include "mk_gemm.h"
 
 namespace mkp {
 
@@ -40,8 +42,9 @@ struct PfArgs {
   const PfCall *call;               // device copy of the call's fields
   int *err;                         // first error code (device)
   float *x, *qkv, *attn;            // chunk scratch (fp32): residual, normed q, attention output
-  float *qkv3, *y3;                 // GEMM outputs as three partials, qkv_stride / y_stride apart
+  float *qkv_p, *y_p;               // GEMM outputs as split-K partials, qkv_stride / y_stride apart
   size_t qkv_stride, y_stride;
+  int qkv_n;                        // partials of the QKV output of the current chunk
   uint16_t *hs;                     // GEMM input as three bf16 terms (hi, mid, lo), hs_stride apart
   size_t hs_stride;
 };
@@ -51,28 +54,41 @@ struct PfLayer {
   const uint16_t *attn_norm, *wq, *wk, *wv, *q_norm, *k_norm, *wo, *mlp_norm, *w_gate, *w_up, *w_down;
 };
 
-// scratch and the GEMM library handle, owned by an mk_handle
+// split-K partials the scratch holds per GEMM output (QKV and gate / up; O and down)
+constexpr int PF_SPLITS_WIDE = 4;
+constexpr int PF_SPLITS_NARROW = 8;
+// captured prefill graphs kept per handle (least recently used replaced)
+constexpr int PF_MAX_GRAPHS = 8;
+
+// scratch and tensor maps, owned by an mk_handle
 struct PfState {
   int tc = 0;                       // tokens per chunk the scratch holds
-  void *blas = nullptr;             // cublasHandle_t
+  int sms = 0;                      // multiprocessors (split-K sizing)
   float *x = nullptr, *qkv = nullptr, *attn = nullptr;
-  float *qkv3 = nullptr, *y3 = nullptr, *gate3 = nullptr, *up3 = nullptr;  // [3][tc][N] GEMM partials
-  float *logits3 = nullptr;         // [3][tc][V], allocated on the first LM head
+  float *qkv_p = nullptr, *y_p = nullptr;  // [splits][tc][N] GEMM partials
+  float *gu_p = nullptr;            // [splits][tc][2 I]: gate columns, then up columns
+  float *logits = nullptr;          // [logit_rows][V], allocated on the first LM head
+  int logit_rows = 0;
   float *pv = nullptr;              // argmax candidates [tc][blocks]
   int *pi = nullptr;
   uint16_t *hs = nullptr;           // [3][tc][kmax] bf16 input terms
   size_t kmax = 0;
   int *err = nullptr;
   PfCall *call = nullptr;           // device copy of the current call
-  void *blas_ws = nullptr;          // GEMM workspace (fixed, so the GEMMs can be captured)
   cudaStream_t cap = nullptr;       // capture stream
+  // TMA tensor maps: per layer {wq, wk, wv}, {wo}, {w_gate, w_up}, {w_down},
+  // then the LM head; the input terms per (K in H, Hq d, I) x (token block 32, 64, 128)
+  std::vector<mkg::WMaps> wmaps;
+  CUtensorMap xmaps[3][3];
   struct Graph {
     int n;
     bool all_logits;
+    unsigned long long used;
     cudaGraph_t graph;
     cudaGraphExec_t exec;
   };
-  std::vector<Graph> graphs;        // captured prefills, one per (n, all_logits)
+  std::vector<Graph> graphs;        // captured prefills, at most PF_MAX_GRAPHS
+  unsigned long long clock = 0;
 };
 
 int pf_init(PfState &st, int tc, int H, int Hq, int Hkv, int d, int I);
