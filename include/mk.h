@@ -145,9 +145,10 @@ typedef struct {
                                  (8 chunks merged by polling up to 1024 cached positions,
                                  then one chunk per 128 positions up to grid / n_kv_heads) */
   int64_t spin_ns;            /* budget of every device wait; 0 = 1 s */
-  int32_t fault_skip_barrier; /* test hook: CTA 0 skips its arrival at the grid barrier
-                                 that closes forward N (0-based, persistent path only);
-                                 -1 = off */
+  int32_t fault_skip_barrier; /* test hook: N > 0 makes CTA 0 skip its arrival at the
+                                 grid barrier that closes forward N - 1 (persistent path
+                                 only), so the other CTAs time out; 0 = off (a zeroed
+                                 struct runs normally) */
   /* Talker inputs summed inside the kernel.  When codes != NULL a negative id
      -(r+1) selects code row r: the forward's input is
        sum_{j<n_books} books[j][codes[r][j]] + text[text_ids[r]]

@@ -64,6 +64,21 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// position in the weight ring: fill index, its slot and the parity of the
+// slot's mbarrier phase (advanced by one per tile, no division)
+struct RingPos {
+  uint32_t it = 0;
+  int slot = 0;
+  uint32_t par = 0;
+  __device__ __forceinline__ void next(int stages) {
+    ++it;
+    if (++slot == stages) {
+      slot = 0;
+      par ^= 1u;
+    }
+  }
+};
+
 // balanced contiguous split of `total` items over G CTAs
 __device__ __forceinline__ void split_range(int total, int G, int cta, int &r0, int &r1) {
   r0 = static_cast<int>((static_cast<long long>(total) * cta) / G);
@@ -213,8 +228,18 @@ __device__ __forceinline__ void ll_settle(const Params &p, SmemCtl &S, const uns
 // stored as KPT/2 word pairs, pair c of every thread side by side, so that
 // each of the consumer's pair loads covers consecutive 16-byte slots of
 // consecutive threads (a warp reads 512 contiguous bytes per load).
+// A staged reader (fast layout 1) polls the vector in natural order.
 __device__ __forceinline__ int ll_slot(const GemvGeom &g, int k) {
-  const int kc = k / g.KPT, j = k - kc * g.KPT;
+  if (g.fast == 1) return k;
+  int kc, j;
+  if (g.fast == 2) {
+    const int c = k >> g.lgSpan, r = k - (c << g.lgSpan);
+    kc = r >> g.lgCH;
+    j = (c << g.lgCH) + (r - (kc << g.lgCH));
+  } else {
+    kc = k / g.KPT;
+    j = k - kc * g.KPT;
+  }
   return (j >> 1) * (2 * g.TPR) + 2 * kc + (j & 1);
 }
 
@@ -415,6 +440,60 @@ __device__ __forceinline__ bool code_row_ok(const Params &p, int r) {
   return t >= 0 && t < p.cb_text_rows;
 }
 
+// Epilogue of one batch of a GEMV phase: one thread per output row (pair)
+// sums the warps' partials of rows a0 .. a0 + nout - 1 from S.red[rb] (pairs:
+// gate rows of a tile, then its up rows) and applies the phase's epilogue:
+// publish, residual add, SiLU(gate) * up, or logits plus a running argmax.
+__device__ __forceinline__ void gemv_epilogue(const Params &p, SmemCtl &S, const GemvGeom &g, int kind, int layer,
+                                              int f, int rb, int a0, int nout, unsigned tag, float &best_v,
+                                              int &best_i) {
+  const int t = threadIdx.x;
+  const int wpr = g.TPR / 32;
+  const int qkv_rows = (p.Hq + 2 * p.Hkv) * p.d;
+  const int own0 = S.rr[kind][0];   // S.xown[0] is row own0 (O and down split H like the residual)
+  // rows go to warps 1.. first: warp 0 shares its scheduler with the producer warp
+  for (int q = (t + NCT - 32) % NCT; q < nout; q += NCT) {
+    const int grow = a0 + q;
+    float y = 0.f;
+    if (kind == GV_GU) {
+      const int qt = g.lgRT >= 0 ? (q >> g.lgRT) : q / g.RT;
+      const int base = qt * 2 * g.RT + (q - qt * g.RT);
+      float up = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < MAX_WPR; ++ww)
+        if (ww < wpr) { y += S.red[rb][base][ww]; up += S.red[rb][base + g.RT][ww]; }
+      ll_store_rep(p, p.ll.u + static_cast<size_t>(layer) * p.I + ll_slot(p.geo[GV_DOWN], grow),
+                   y / (1.0f + expf(-y)) * up, tag);
+      continue;
+    }
+#pragma unroll
+    for (int ww = 0; ww < MAX_WPR; ++ww)
+      if (ww < wpr) y += S.red[rb][q][ww];
+    switch (kind) {
+      case GV_QKV: ll_store_rep(p, p.ll.qkv + static_cast<size_t>(layer) * qkv_rows + grow, y, tag); break;
+      case GV_O: {
+        const float xn = S.xown[grow - own0] + y;
+        S.xown[grow - own0] = xn;
+        ll_store_rep(p, p.ll.xmid + static_cast<size_t>(layer) * p.H + ll_slot(p.geo[GV_GU], grow), xn, tag);
+        break;
+      }
+      case GV_DOWN: {
+        const float xn = S.xown[grow - own0] + y;
+        S.xown[grow - own0] = xn;
+        ll_store_rep(p, p.ll.xout + static_cast<size_t>(layer) * p.H + ll_slot(p.geo[GV_QKV], grow), xn, tag);
+        if (p.hidden) p.hidden[(static_cast<size_t>(f) * (p.L + 1) + layer + 1) * p.H + grow] = xn;
+        break;
+      }
+      default: {  // LM head
+        if (p.logits) p.logits[static_cast<size_t>(f) * p.V + grow] = y;
+        if (!isfinite(y)) set_err(p, MK_ERR_NUMERIC_D);
+        if (y > best_v) { best_v = y; best_i = grow; }
+        break;
+      }
+    }
+  }
+}
+
 // One GEMV phase of this CTA: y[r] = W[r,:] . in for the CTA's rows, with the
 // RMSNorm of the input fused in (QKV, gate/up, LM head) and the phase's
 // epilogue (publish, residual add, SiLU*mul, logits + argmax candidate).
@@ -422,13 +501,12 @@ __device__ __forceinline__ bool code_row_ok(const Params &p, int r) {
 // batch buffer and one barrier per batch precedes the epilogue.
 template <int KPT, int RPTP>
 __device__ __noinline__ void gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer, int f,
-                           int cta, int in_id, unsigned tag, uint32_t &it, int &rb, int gp) {
+                           int cta, int in_id, unsigned tag, RingPos &rp, int &rb, int gp) {
   const GemvGeom g = p.geo[kind];
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int kc = t % g.TPR, rg = t / g.TPR;
   const int k0 = kc * KPT;
   const bool norm = (kind == GV_QKV || kind == GV_GU || kind == GV_LM);
-  const int qkv_rows = (p.Hq + 2 * p.Hkv) * p.d;
 
   // ---- gains (independent of the input: their latency overlaps the poll) ---
   float gn[KPT];
@@ -464,17 +542,16 @@ __device__ __noinline__ void gemv_phase(const Params &p, SmemCtl &S, unsigned ch
     float tot = 0.f;
 #pragma unroll
     for (int i = 0; i < NCW; ++i) tot += S.misc[i];
-    const float rs = 1.0f / sqrtf(tot / static_cast<float>(g.K) + p.eps);
+    const float ms = g.invK != 0.f ? tot * g.invK : tot / static_cast<float>(g.K);   // identical for 2^n
+    const float rs = 1.0f / sqrtf(ms + p.eps);
 #pragma unroll
     for (int j = 0; j < KPT; ++j) xr[j] = xr[j] * rs * gn[j];
   }
 
-  int r0, r1;
-  split_range(g.rows, p.G, cta, r0, r1);
+  const int r0 = S.rr[kind][0], r1 = S.rr[kind][1];
   // the first layer's input also seeds the residual rows this CTA owns
   if (kind == GV_QKV && layer == 0) {
-    int o0, o1;
-    split_range(p.H, p.G, cta, o0, o1);
+    const int o0 = S.rr[GV_O][0], o1 = S.rr[GV_O][1];
     for (int r = o0 + t; r < o1; r += NCT) {
       const float v = input_elem(p, in_id, r);
       S.xown[r - o0] = v;
@@ -498,10 +575,9 @@ __device__ __noinline__ void gemv_phase(const Params &p, SmemCtl &S, unsigned ch
       const int a = r0 + ti * g.RT;
       const int nr = min(g.RT, r1 - a);
       const int rows_in_tile = (kind == GV_GU) ? 2 * nr : nr;
-      const int slot = static_cast<int>(it % static_cast<uint32_t>(p.stages));
-      const uint32_t par = (it / static_cast<uint32_t>(p.stages)) & 1u;
-      wait_full(p, S, slot, par);
-      const unsigned char *st = ring + static_cast<size_t>(slot) * p.stage_bytes;
+      const int slot = rp.slot;
+      wait_full(p, S, slot, rp.par);
+      const unsigned char *st = ring + static_cast<size_t>(slot) * STAGE_BYTES;
       // every row slot computes a dot product (slots past the tile's last row
       // re-read that row and are zeroed) so that no branch separates the rows
       // and their load/FMA chains interleave
@@ -523,52 +599,11 @@ __device__ __noinline__ void gemv_phase(const Params &p, SmemCtl &S, unsigned ch
         else brow = (ti - tb) * g.RT + row;
         S.red[rb][brow][wg] = v;
       }
-      ++it;
+      rp.next(p.stages);
     }
     cons_sync();
-    // ---- epilogue of the batch: one thread per output row (pair) ------------
-    const int a0 = r0 + tb * g.RT;
-    const int nout = min(r1, r0 + te * g.RT) - a0;
-    // rows go to warps 1.. first: warp 0 shares its scheduler with the producer warp
-    for (int q = (t + NCT - 32) % NCT; q < nout; q += NCT) {
-      const int grow = a0 + q;
-      float y = 0.f;
-      if (kind == GV_GU) {
-        const int base = (q / g.RT) * 2 * g.RT + (q % g.RT);
-        float up = 0.f;
-#pragma unroll
-        for (int ww = 0; ww < MAX_WPR; ++ww)
-          if (ww < wpr) { y += S.red[rb][base][ww]; up += S.red[rb][base + g.RT][ww]; }
-        ll_store_rep(p, p.ll.u + static_cast<size_t>(layer) * p.I + ll_slot(p.geo[GV_DOWN], grow),
-                     y / (1.0f + expf(-y)) * up, tag);
-        continue;
-      }
-#pragma unroll
-      for (int ww = 0; ww < MAX_WPR; ++ww)
-        if (ww < wpr) y += S.red[rb][q][ww];
-      switch (kind) {
-        case GV_QKV: ll_store_rep(p, p.ll.qkv + static_cast<size_t>(layer) * qkv_rows + grow, y, tag); break;
-        case GV_O: {
-          const float xn = S.xown[grow - r0] + y;
-          S.xown[grow - r0] = xn;
-          ll_store_rep(p, p.ll.xmid + static_cast<size_t>(layer) * p.H + ll_slot(p.geo[GV_GU], grow), xn, tag);
-          break;
-        }
-        case GV_DOWN: {
-          const float xn = S.xown[grow - r0] + y;
-          S.xown[grow - r0] = xn;
-          ll_store_rep(p, p.ll.xout + static_cast<size_t>(layer) * p.H + ll_slot(p.geo[GV_QKV], grow), xn, tag);
-          if (p.hidden) p.hidden[(static_cast<size_t>(f) * (p.L + 1) + layer + 1) * p.H + grow] = xn;
-          break;
-        }
-        default: {  // LM head
-          if (p.logits) p.logits[static_cast<size_t>(f) * p.V + grow] = y;
-          if (!isfinite(y)) set_err(p, MK_ERR_NUMERIC_D);
-          if (y > best_v) { best_v = y; best_i = grow; }
-          break;
-        }
-      }
-    }
+    gemv_epilogue(p, S, g, kind, layer, f, rb, r0 + tb * g.RT, min(r1, r0 + te * g.RT) - (r0 + tb * g.RT), tag,
+                  best_v, best_i);
     rb ^= 1;
   }
   // the warps without epilogue rows wait here instead of starting the next
@@ -586,12 +621,300 @@ __device__ __noinline__ void gemv_phase(const Params &p, SmemCtl &S, unsigned ch
   trace_mark(p, gp, cta, 2);
 }
 
+// ---------------------------------------------------------------------------
+// fast GEMV layouts (GemvGeom::fast 1 and 2)
+// ---------------------------------------------------------------------------
+// dot of one bf16 row in shared memory with the thread's slice in the chunked
+// layout: chunk c of thread kc holds the CH elements from c*SPAN + kc*CH, so
+// every load of a warp covers consecutive bytes.  One accumulator per chunk,
+// summed in chunk order.
+template <int KPT, int CH, int SPAN>
+__device__ __forceinline__ float dot_chunked(const unsigned char *row, int kc, const float (&xr)[KPT]) {
+  constexpr int NCH = KPT / CH;
+  float s[NCH];
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    const unsigned char *q = row + (c * SPAN + kc * CH) * 2;
+    float a = 0.f;
+    if constexpr (CH == 8) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(q);
+      a = fmaf(bf_lo(v.x), xr[8 * c + 0], a);
+      a = fmaf(bf_hi(v.x), xr[8 * c + 1], a);
+      a = fmaf(bf_lo(v.y), xr[8 * c + 2], a);
+      a = fmaf(bf_hi(v.y), xr[8 * c + 3], a);
+      a = fmaf(bf_lo(v.z), xr[8 * c + 4], a);
+      a = fmaf(bf_hi(v.z), xr[8 * c + 5], a);
+      a = fmaf(bf_lo(v.w), xr[8 * c + 6], a);
+      a = fmaf(bf_hi(v.w), xr[8 * c + 7], a);
+    } else {
+      const uint2 v = *reinterpret_cast<const uint2 *>(q);
+      a = fmaf(bf_lo(v.x), xr[4 * c + 0], a);
+      a = fmaf(bf_hi(v.x), xr[4 * c + 1], a);
+      a = fmaf(bf_lo(v.y), xr[4 * c + 2], a);
+      a = fmaf(bf_hi(v.y), xr[4 * c + 3], a);
+    }
+    s[c] = a;
+  }
+  float r = s[0];
+#pragma unroll
+  for (int c = 1; c < NCH; ++c) r += s[c];
+  return r;
+}
+
+// Poll n (<= MP) word pairs src[c * stride], src[c * stride + 1] until they
+// carry `tag`; pairs c >= n read as zero.  Only stale words are reloaded.
+template <int MP>
+__device__ __forceinline__ void ll_poll_pairs(const Params &p, SmemCtl &S, const unsigned long long *src, int stride,
+                                              int n, unsigned tag, float (&v)[2 * MP]) {
+  unsigned stale = 0;
+#pragma unroll
+  for (int c = 0; c < MP; ++c) {
+    v[2 * c] = v[2 * c + 1] = 0.f;
+    if (c < n) {
+      unsigned long long a, b;
+      ll_load2(src + c * stride, a, b);
+      v[2 * c] = ll_val(a);
+      v[2 * c + 1] = ll_val(b);
+      stale |= (ll_tag(a) != tag ? 1u : 0u) << (2 * c);
+      stale |= (ll_tag(b) != tag ? 1u : 0u) << (2 * c + 1);
+    }
+  }
+  if (stale == 0) return;
+  Deadline dl;
+  int k = 0;
+  for (;;) {
+#pragma unroll
+    for (int j = 0; j < 2 * MP; ++j) {
+      if (stale & (1u << j)) {
+        const unsigned long long wj = ll_load(src + (j >> 1) * stride + (j & 1));
+        if (ll_tag(wj) == tag) {
+          v[j] = ll_val(wj);
+          stale &= ~(1u << j);
+        }
+      }
+    }
+    if (stale == 0) return;
+    if ((++k & 15) == 0) {
+      if (flag(S, F_ABORT) || ld_relaxed_i32(p.err) != 0) return;
+      if (dl.expired(p.spin_ns)) {
+        set_err(p, MK_ERR_TIMEOUT_D);
+        flag(S, F_ABORT) = 1;
+        return;
+      }
+    }
+  }
+}
+
+// One GEMV phase in a fast layout.  STAGED (layout 1): TPR = 32, row group =
+// warp; the input vector is polled once per CTA into S.xs in natural order
+// (thread t the word pairs at 2t + 512 m), its RMSNorm reduced on the way,
+// and every warp then reads its chunks of the whole vector from S.xs.  Split-K
+// (layout 2): TPR = 256, one row group; each thread polls its own chunks.
+// Either way a thread keeps the partial dots of RPT rows of BT tiles in
+// registers and the warp reduces them once per batch; the partials of the
+// warps sharing a row (layout 2) meet in S.red before the epilogue.
+template <int KPT, int RPT, int BT, bool STAGED>
+__device__ __noinline__ void gemv_fast(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer, int f,
+                                       int cta, int in_id, unsigned tag, RingPos &rp, int &rb, int gp) {
+  constexpr int CH = (KPT % 8 == 0) ? 8 : 4;
+  constexpr int TPR = STAGED ? 32 : NCT;
+  constexpr int NG = NCT / TPR;
+  constexpr int SPAN = TPR * CH;
+  constexpr int NS = RPT * BT;
+  constexpr int LOGN = (NS >= 32) ? 5 : (NS >= 16) ? 4 : (NS >= 8) ? 3 : (NS >= 4) ? 2 : (NS >= 2) ? 1 : 0;
+  static_assert((NS & (NS - 1)) == 0 && NS <= 32, "slots per batch: a power of two up to 32");
+  const GemvGeom g = p.geo[kind];
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int kc = t % TPR, rg = t / TPR;
+  const int wg = w % (TPR / 32);
+
+  float xr[KPT];
+  if constexpr (STAGED) {
+    // ---- gains of this lane's chunks (the loads overlap the poll) ----------
+    const uint16_t *gain = kind == GV_QKV ? S.layers[layer].attn_norm
+                         : kind == GV_GU  ? S.layers[layer].mlp_norm
+                                          : p.final_norm;
+    float gn[KPT];
+#pragma unroll
+    for (int c = 0; c < KPT / CH; ++c) {
+      float v[CH];
+      load_bf16<CH>(gain + c * SPAN + kc * CH, v);
+#pragma unroll
+      for (int j = 0; j < CH; ++j) gn[c * CH + j] = v[j];
+    }
+    // ---- the input vector into S.xs, with its sum of squares ---------------
+    constexpr int MP = (KPT * 32 + 511) / 512;   // word pairs per thread
+    const int np = (g.K - 2 * t + 511) / 512;    // pairs of this thread inside the vector
+    float v[2 * MP];
+    if (kind == GV_QKV && layer == 0) {
+#pragma unroll
+      for (int c = 0; c < MP; ++c) {
+        v[2 * c] = v[2 * c + 1] = 0.f;
+        if (c < np) {
+          v[2 * c] = input_elem(p, in_id, 2 * t + 512 * c);
+          v[2 * c + 1] = input_elem(p, in_id, 2 * t + 512 * c + 1);
+        }
+      }
+    } else {
+      const unsigned long long *src =
+          kind == GV_QKV ? p.ll.xout + static_cast<size_t>(layer - 1) * p.H
+        : kind == GV_GU  ? p.ll.xmid + static_cast<size_t>(layer) * p.H
+                         : p.ll.xout + static_cast<size_t>(p.L - 1) * p.H;
+      ll_poll_pairs<MP>(p, S, src + (cta % p.ll_rep) * p.ll_cs + 2 * t, 512, np, tag, v);
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int c = 0; c < MP; ++c) {
+      if (c < np) {
+        *reinterpret_cast<float2 *>(&S.xs[2 * t + 512 * c]) = make_float2(v[2 * c], v[2 * c + 1]);
+        ss = fmaf(v[2 * c], v[2 * c], ss);
+        ss = fmaf(v[2 * c + 1], v[2 * c + 1], ss);
+      }
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) S.misc[w] = ss;
+    cons_sync();
+    float tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < NCW; ++i) tot += S.misc[i];
+    const float ms = g.invK != 0.f ? tot * g.invK : tot / static_cast<float>(g.K);   // identical for 2^n
+    const float rs = 1.0f / sqrtf(ms + p.eps);
+#pragma unroll
+    for (int c = 0; c < KPT / CH; ++c) {
+#pragma unroll
+      for (int j = 0; j < CH; j += 4) {
+        const float4 q = *reinterpret_cast<const float4 *>(&S.xs[c * SPAN + kc * CH + j]);
+        xr[c * CH + j + 0] = q.x * rs * gn[c * CH + j + 0];
+        xr[c * CH + j + 1] = q.y * rs * gn[c * CH + j + 1];
+        xr[c * CH + j + 2] = q.z * rs * gn[c * CH + j + 2];
+        xr[c * CH + j + 3] = q.w * rs * gn[c * CH + j + 3];
+      }
+    }
+  } else {
+    const unsigned long long *src = kind == GV_O ? p.ll.attn + static_cast<size_t>(layer) * p.Hq * p.d
+                                                 : p.ll.u + static_cast<size_t>(layer) * p.I;
+    ll_poll_slice<KPT>(p, S, src + (cta % p.ll_rep) * p.ll_cs + 2 * kc, 2 * TPR, tag, xr);
+  }
+
+  const int r0 = S.rr[kind][0], r1 = S.rr[kind][1];
+  // the first layer's input also seeds the residual rows this CTA owns
+  if (kind == GV_QKV && layer == 0) {
+    const int o0 = S.rr[GV_O][0], o1 = S.rr[GV_O][1];
+    for (int r = o0 + t; r < o1; r += NCT) {
+      const float x0 = input_elem(p, in_id, r);
+      S.xown[r - o0] = x0;
+      if (p.hidden) p.hidden[(static_cast<size_t>(f) * (p.L + 1)) * p.H + r] = x0;
+    }
+  }
+  trace_mark(p, gp, cta, 1);
+
+  const int ntiles = (r1 - r0 + g.RT - 1) / g.RT;
+  const int trow = (kind == GV_GU) ? 2 * g.RT : g.RT;       // rows of a full tile
+  const size_t rowb = static_cast<size_t>(g.K) * 2;
+  float best_v = -INFINITY;
+  int best_i = INT_MAX;
+  for (int tb = 0; tb < ntiles; tb += BT) {
+    const int te = min(ntiles, tb + BT);
+    float acc[NS];
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+      const int ti = tb + b;
+      if (ti < te) {
+        const int nr = min(g.RT, r1 - (r0 + ti * g.RT));
+        const int rit = (kind == GV_GU) ? 2 * nr : nr;      // rows in this tile
+        const int slot = rp.slot;
+        wait_full(p, S, slot, rp.par);
+        const unsigned char *st = ring + static_cast<size_t>(slot) * STAGE_BYTES;
+        // row slots past the tile's last row re-read that row and are zeroed
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+          const int row = rg + i * NG;
+          const int rr = min(row, rit - 1);
+          const float dv = dot_chunked<KPT, CH, SPAN>(st + rr * rowb, kc, xr);
+          acc[b * RPT + i] = row < rit ? dv : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[slot]);
+        rp.next(p.stages);
+      } else {
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) acc[b * RPT + i] = 0.f;
+      }
+    }
+    const float v = warp_multi_reduce<NS>(acc, lane);
+    if constexpr (STAGED) {
+      if (kind == GV_QKV || kind == GV_LM) {
+        // a warp owns whole rows: the lane holding a row's sum publishes it
+        // itself (no partials to combine, no batch barrier)
+        const int sl = lane >> (5 - LOGN);
+        const int b = sl / RPT, i = sl % RPT;
+        const int ti = tb + b;
+        if ((lane & ((32 >> LOGN) - 1)) == 0 && ti < te) {
+          const int nr = min(g.RT, r1 - (r0 + ti * g.RT));
+          const int row = rg + i * NG;
+          if (row < nr) {
+            const int grow = r0 + ti * g.RT + row;
+            if (kind == GV_QKV) {
+              ll_store_rep(p, p.ll.qkv + static_cast<size_t>(layer) * ((p.Hq + 2 * p.Hkv) * p.d) + grow, v, tag);
+            } else {
+              if (p.logits) p.logits[static_cast<size_t>(f) * p.V + grow] = v;
+              if (!isfinite(v)) set_err(p, MK_ERR_NUMERIC_D);
+              if (v > best_v || (v == best_v && grow < best_i)) { best_v = v; best_i = grow; }
+            }
+          }
+        }
+        continue;
+      }
+    }
+    {
+      const int sl = lane >> (5 - LOGN);                    // slot this lane holds
+      const int b = sl / RPT, i = sl % RPT;
+      const int ti = tb + b;
+      if ((lane & ((32 >> LOGN) - 1)) == 0 && ti < te) {
+        const int nr = min(g.RT, r1 - (r0 + ti * g.RT));
+        const int rit = (kind == GV_GU) ? 2 * nr : nr;
+        const int row = rg + i * NG;
+        if (row < rit)
+          S.red[rb][b * trow + ((kind == GV_GU && row >= nr) ? g.RT + (row - nr) : row)][wg] = v;
+      }
+    }
+    cons_sync();
+    gemv_epilogue(p, S, g, kind, layer, f, rb, r0 + tb * g.RT, min(r1, r0 + te * g.RT) - (r0 + tb * g.RT), tag,
+                  best_v, best_i);
+    rb ^= 1;
+  }
+  // warps without epilogue rows wait for the publishing ones (see gemv_phase)
+  cons_sync();
+
+  if (kind == GV_LM) {
+    block_argmax(S, best_v, best_i);
+    if (t == 0) {
+      p.cand_val[cta] = best_v;
+      p.cand_idx[cta] = best_i;
+    }
+  }
+  trace_mark(p, gp, cta, 2);
+}
+
 // dispatch on (KPT, RPTP) fixed at mk_create
 static __device__ __noinline__ void gemv_dispatch(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer, int f,
-                              int cta, int in_id, unsigned tag, uint32_t &it, int &rb, int gp) {
+                              int cta, int in_id, unsigned tag, RingPos &rp, int &rb, int gp) {
   const int kpt = p.geo[kind].KPT, r = p.geo[kind].RPTP;
+  if (p.geo[kind].fast) {
+    // the fast layouts mk_create may pick (KPT, rows per thread per tile, tiles per batch)
+    const int bt = p.geo[kind].BT;
+#define MK_FAST_CASE(ST, KP, RP, B) \
+  if (p.geo[kind].fast == (ST ? 1 : 2) && kpt == KP && r == RP && bt == B) { \
+    gemv_fast<KP, RP, B, ST>(p, S, ring, kind, layer, f, cta, in_id, tag, rp, rb, gp); return; }
+    MK_FAST_CASE(true, 32, 2, 4) MK_FAST_CASE(true, 64, 1, 8) MK_FAST_CASE(true, 16, 4, 2)
+    MK_FAST_CASE(true, 24, 2, 4) MK_FAST_CASE(true, 8, 8, 1)
+    MK_FAST_CASE(false, 8, 8, 1) MK_FAST_CASE(false, 8, 8, 2) MK_FAST_CASE(false, 12, 4, 2)
+    MK_FAST_CASE(false, 24, 2, 8)
+#undef MK_FAST_CASE
+    return;
+  }
 #define MK_GEMV_CASE(KP, RP) \
-  if (kpt == KP && r == RP) { gemv_phase<KP, RP>(p, S, ring, kind, layer, f, cta, in_id, tag, it, rb, gp); return; }
+  if (kpt == KP && r == RP) { gemv_phase<KP, RP>(p, S, ring, kind, layer, f, cta, in_id, tag, rp, rb, gp); return; }
   // every (KPT, RPTP) with KPT * RPTP <= 128 (mk_create rejects the others)
   MK_GEMV_CASE(8, 1) MK_GEMV_CASE(8, 2) MK_GEMV_CASE(8, 4) MK_GEMV_CASE(8, 8) MK_GEMV_CASE(8, 16)
   MK_GEMV_CASE(12, 1) MK_GEMV_CASE(12, 2) MK_GEMV_CASE(12, 4) MK_GEMV_CASE(12, 8)
@@ -746,12 +1069,11 @@ static __device__ __noinline__ float merge_polled_chunks(const Params &p, SmemCt
 
 template <int HD, int GRP>
 __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring, int l, int f, int cta,
-                                unsigned tag, uint32_t &it, int gp) {
+                                unsigned tag, RingPos &rp, int gp, const AttnSched &as) {
   constexpr int EPL = HD / 32;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  const AttnSched as = attn_sched(p, f);
   const int P = as.P;
-  const int TP = p.stage_bytes / (4 * HD);     // positions per ring tile (K rows + V rows)
+  constexpr int TP = STAGE_BYTES / (4 * HD);   // positions per ring tile (K rows + V rows)
   // polled merge needs every unit on its own CTA (a CTA never waits for itself)
   const bool poll_merge = as.C > 1 && as.C <= p.poll_cm && as.units <= p.G;
   const LayerPtrs &LW = S.layers[l];
@@ -850,10 +1172,9 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
     };
     for (int p0 = a; p0 < pend; p0 += TP) {
       const int np = min(TP, pend - p0);
-      const int slot = static_cast<int>(it % static_cast<uint32_t>(p.stages));
-      const uint32_t par = (it / static_cast<uint32_t>(p.stages)) & 1u;
-      wait_full(p, S, slot, par);
-      const unsigned char *st = ring + static_cast<size_t>(slot) * p.stage_bytes;
+      const int slot = rp.slot;
+      wait_full(p, S, slot, rp.par);
+      const unsigned char *st = ring + static_cast<size_t>(slot) * STAGE_BYTES;
       const uint16_t *kt = reinterpret_cast<const uint16_t *>(st) + lane * EPL;
       const uint16_t *vt = kt + static_cast<size_t>(np) * HD;
       int i = w;
@@ -884,7 +1205,7 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[slot]);
-      ++it;
+      rp.next(p.stages);
     }
     if (has_cur && w == NCW - 1) {
       float kk[EPL], vv[EPL];
@@ -971,12 +1292,12 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
 
 template <int HD>
 __device__ void attention_dispatch(const Params &p, SmemCtl &S, unsigned char *ring, int l, int f, int cta,
-                                   unsigned tag, uint32_t &it, int gp) {
+                                   unsigned tag, RingPos &rp, int gp, const AttnSched &as) {
   switch (p.grp) {
-    case 1: attention_phase<HD, 1>(p, S, ring, l, f, cta, tag, it, gp); break;
-    case 2: attention_phase<HD, 2>(p, S, ring, l, f, cta, tag, it, gp); break;
-    case 4: attention_phase<HD, 4>(p, S, ring, l, f, cta, tag, it, gp); break;
-    default: if constexpr (HD * 8 <= MAX_GRP_HD) attention_phase<HD, 8>(p, S, ring, l, f, cta, tag, it, gp); break;
+    case 1: attention_phase<HD, 1>(p, S, ring, l, f, cta, tag, rp, gp, as); break;
+    case 2: attention_phase<HD, 2>(p, S, ring, l, f, cta, tag, rp, gp, as); break;
+    case 4: attention_phase<HD, 4>(p, S, ring, l, f, cta, tag, rp, gp, as); break;
+    default: if constexpr (HD * 8 <= MAX_GRP_HD) attention_phase<HD, 8>(p, S, ring, l, f, cta, tag, rp, gp, as); break;
   }
 }
 
@@ -988,8 +1309,10 @@ struct Producer {
   SmemCtl &S;
   unsigned char *ring;
   uint64_t pol_w, pol_kv;
-  uint32_t it = 0;
+  RingPos rp;
   bool stop = false;
+  AttnSched as;
+  int as_f = -1;
 
   __device__ Producer(const Params &pp, SmemCtl &SS, unsigned char *r) : p(pp), S(SS), ring(r) {
     pol_w = policy_evict_first();
@@ -998,10 +1321,10 @@ struct Producer {
 
   // claim the next ring slot (waits until the consumers released it)
   __device__ unsigned char *claim(int &slot) {
-    slot = static_cast<int>(it % static_cast<uint32_t>(p.stages));
-    const uint32_t k = it / static_cast<uint32_t>(p.stages);
-    if (k > 0) {
-      const uint32_t par = (k - 1) & 1u;
+    slot = rp.slot;
+    if (rp.it >= static_cast<uint32_t>(p.stages)) {
+      const uint32_t par = rp.par ^ 1u;                       // the slot's previous fill
+
       if (!mbar_try_wait(&S.empty[slot], par)) {
         Deadline dl;
         int n = 0;
@@ -1014,13 +1337,12 @@ struct Producer {
       }
     }
     if (flag(S, F_ABORT)) { stop = true; return nullptr; }
-    return ring + static_cast<size_t>(slot) * p.stage_bytes;
+    return ring + static_cast<size_t>(slot) * STAGE_BYTES;
   }
 
   __device__ void gemv_tiles(int kind, int layer, int cta) {
     const GemvGeom g = p.geo[kind];
-    int r0, r1;
-    split_range(g.rows, p.G, cta, r0, r1);
+    const int r0 = S.rr[kind][0], r1 = S.rr[kind][1];
     const uint32_t rowb = static_cast<uint32_t>(g.K) * 2u;
     for (int a = r0; a < r1 && !stop; a += g.RT) {
       const int nr = min(g.RT, r1 - a);
@@ -1063,14 +1385,55 @@ struct Producer {
         bulk_load(dst + off, src[i], bytes[i], &S.full[slot], pol_w);
         off += bytes[i];
       }
-      ++it;
+      rp.next(p.stages);
     }
+  }
+
+  // Prefetch this CTA's weight rows of a later GEMV phase into L2 (at most
+  // PREFETCH_MAX bytes per matrix range), so that its ring fills come from L2
+  // rather than from HBM: the ring alone holds only a few tiles ahead.
+  static constexpr uint32_t PREFETCH_MAX = 256 * 1024;
+  __device__ void prefetch_range(const uint16_t *src, uint32_t bytes) {
+    bulk_prefetch_l2(src, bytes < PREFETCH_MAX ? bytes : PREFETCH_MAX);
+  }
+  __device__ void prefetch_phase(int kind, int layer) {
+    const GemvGeom &g = p.geo[kind];
+    const int r0 = S.rr[kind][0], r1 = S.rr[kind][1];
+    if (r1 <= r0) return;
+    const uint32_t rowb = static_cast<uint32_t>(g.K) * 2u;
+    const LayerPtrs &L = S.layers[layer];
+    if (kind == GV_QKV) {
+      const int qr = p.Hq * p.d, kr = p.Hkv * p.d;
+      const int segs[4] = {0, qr, qr + kr, qr + 2 * kr};
+      const uint16_t *mats[3] = {L.wq, L.wk, L.wv};
+#pragma unroll
+      for (int s = 0; s < 3; ++s) {
+        const int lo = max(r0, segs[s]), hi = min(r1, segs[s + 1]);
+        if (lo < hi) prefetch_range(mats[s] + static_cast<size_t>(lo - segs[s]) * g.K, (hi - lo) * rowb);
+      }
+    } else if (kind == GV_GU) {
+      prefetch_range(L.w_gate + static_cast<size_t>(r0) * g.K, (r1 - r0) * rowb);
+      prefetch_range(L.w_up + static_cast<size_t>(r0) * g.K, (r1 - r0) * rowb);
+    } else {
+      const uint16_t *base = kind == GV_O ? L.wo : kind == GV_DOWN ? L.w_down : p.lm_head;
+      prefetch_range(base + static_cast<size_t>(r0) * g.K, (r1 - r0) * rowb);
+    }
+  }
+  // the GEMV phase ph of a forward (attention phases have no weights: -1)
+  __device__ void prefetch_ph(int ph) {
+    if (ph == 5 * p.L) { prefetch_phase(GV_LM, 0); return; }
+    const int l = ph / 5, k = ph - 5 * l;
+    if (k == 1) return;
+    prefetch_phase(k == 0 ? GV_QKV : k == 2 ? GV_O : k == 3 ? GV_GU : GV_DOWN, l);
   }
 
   template <int HD>
   __device__ void kv_tiles(int l, int f, int cta) {
-    const AttnSched as = attn_sched(p, f);
-    const int TP = p.stage_bytes / (4 * HD);
+    if (as_f != f) {
+      as = attn_sched(p, f);
+      as_f = f;
+    }
+    constexpr int TP = STAGE_BYTES / (4 * HD);
     bool guarded = false;
     for (int u = cta; u < as.units && !stop; u += p.G) {
       const int g = u / as.C, c = u % as.C;
@@ -1103,7 +1466,7 @@ struct Producer {
         mbar_arrive_expect_tx(&S.full[slot], 2u * bytes);
         bulk_load(dst, p.kcache + row0 * HD, bytes, &S.full[slot], pol_kv);
         bulk_load(dst + bytes, p.vcache + row0 * HD, bytes, &S.full[slot], pol_kv);
-        ++it;
+        rp.next(p.stages);
       }
     }
   }
@@ -1111,6 +1474,7 @@ struct Producer {
   // wait for every copy this producer issued (each slot's latest fill)
   __device__ void drain() {
     const uint32_t ns = static_cast<uint32_t>(p.stages);
+    const uint32_t it = rp.it;
     const uint32_t used = it < ns ? it : ns;
     for (uint32_t s = 0; s < used; ++s) {
       const uint32_t last = ((it - 1 - s) / ns) * ns + s;     // largest fill index of slot s
@@ -1183,6 +1547,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
       mbar_init(&S.empty[s], NCW);
     }
     fence_mbar_init();
+    // this CTA's rows of every GEMV phase (the O and down ranges are also the
+    // residual rows it owns), computed once instead of in every phase
+    for (int k = 0; k < GV_COUNT; ++k) split_range(p.geo[k].rows, p.G, cta, S.rr[k][0], S.rr[k][1]);
     flag(S, F_ABORT) = (p.per_op && ld_relaxed_i32(p.err) != 0) ? 1 : 0;
     flag(S, F_PROD_DONE) = 0;
     flag(S, F_FWD_DONE) = p.per_op ? INT_MAX : 0;
@@ -1200,9 +1567,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
 
   int gp_begin, gp_end;
   bool final_select;
+  // (forward, phase) of gp_begin, advanced with gp (no division in the loop)
+  int f0 = 0, ph0 = 0;
   if (p.per_op) {
     if (p.op_phase >= NPH) { gp_begin = gp_end = 0; final_select = true; }
-    else { gp_begin = p.op_fwd * NPH + p.op_phase; gp_end = gp_begin + 1; final_select = false; }
+    else {
+      gp_begin = p.op_fwd * NPH + p.op_phase;
+      gp_end = gp_begin + 1;
+      final_select = false;
+      f0 = p.op_fwd;
+      ph0 = p.op_phase;
+    }
   } else {
     gp_begin = 0;
     gp_end = p.n_fwd * NPH;
@@ -1213,17 +1588,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
     // ---------------- producer warp (lane 0 issues everything) ----------------
     if (lane == 0) {
       Producer pr(p, S, ring);
+      int f = f0, ph = ph0;
+      // weights of the phases PF_AHEAD ahead are prefetched into L2 (persistent path)
+      constexpr int PF_AHEAD = 2;
+      if (!p.per_op)
+        for (int a = 0; a < PF_AHEAD && gp_begin + a < gp_end; ++a) pr.prefetch_ph((ph0 + a) % NPH);
       for (int gp = gp_begin; gp < gp_end && !pr.stop; ++gp) {
-        const int f = gp / NPH, ph = gp % NPH;
-        if (ph == 5 * p.L) { pr.gemv_tiles(GV_LM, 0, cta); continue; }
-        const int l = ph / 5;
-        switch (ph % 5) {
-          case 0: pr.gemv_tiles(GV_QKV, l, cta); break;
-          case 1: pr.kv_tiles<HD>(l, f, cta); break;
-          case 2: pr.gemv_tiles(GV_O, l, cta); break;
-          case 3: pr.gemv_tiles(GV_GU, l, cta); break;
-          default: pr.gemv_tiles(GV_DOWN, l, cta); break;
+        if (!p.per_op && gp + PF_AHEAD < gp_end) {
+          int pa = ph + PF_AHEAD;
+          if (pa >= NPH) pa -= NPH;
+          pr.prefetch_ph(pa);
         }
+        if (ph == 5 * p.L) {
+          pr.gemv_tiles(GV_LM, 0, cta);
+        } else {
+          const int l = ph / 5;
+          switch (ph - 5 * l) {
+            case 0: pr.gemv_tiles(GV_QKV, l, cta); break;
+            case 1: pr.kv_tiles<HD>(l, f, cta); break;
+            case 2: pr.gemv_tiles(GV_O, l, cta); break;
+            case 3: pr.gemv_tiles(GV_GU, l, cta); break;
+            default: pr.gemv_tiles(GV_DOWN, l, cta); break;
+          }
+        }
+        if (++ph == NPH) { ph = 0; ++f; }
       }
       pr.drain();
       st_release_cta(&S.flags[F_PROD_DONE], 1);
@@ -1235,23 +1623,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
   // Phases hand their outputs to the next phase as tagged words (no barrier);
   // only the LM head ends with a grid barrier, which publishes the argmax
   // candidates and orders this forward's KV-cache writes before the next one.
-  uint32_t it = 0;
+  RingPos rp;
   int rb = 0;
   unsigned bar_target = 0;
   int in_id = 0;
   bool ok = true;
-  for (int gp = gp_begin; gp < gp_end && ok; ++gp) {
-    const int f = gp / NPH, ph = gp % NPH;
+  AttnSched as;                 // the split-KV schedule of forward as_f (the same for all its layers)
+  int as_f = -1;
+  int f = f0, ph = ph0;
+  for (int gp = gp_begin; gp < gp_end && ok; ++gp, (++ph == NPH) ? (ph = 0, ++f) : 0) {
     const unsigned tag = p.tag0 + static_cast<unsigned>(f);
     trace_mark(p, gp, cta, 0);
     if (ph == 5 * p.L) {
-      gemv_dispatch(p, S, ring, GV_LM, 0, f, cta, in_id, tag, it, rb, gp);
+      gemv_dispatch(p, S, ring, GV_LM, 0, f, cta, in_id, tag, rp, rb, gp);
       if (!p.per_op) {
         ok = grid_barrier(p, S, bar_target, f, cta);
         if (tid == 0) st_release_cta(&S.flags[F_FWD_DONE], f + 1);
       }
     } else {
-      const int l = ph / 5, k = ph % 5;
+      const int l = ph / 5, k = ph - 5 * l;
       if (k == 0 && l == 0) {
         // the token of this forward: teacher-forced input, or fed back in-kernel
         int prev = 0;
@@ -1270,12 +1660,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
         }
         in_id = id;
       }
+      if (k == 1 && as_f != f) {
+        as = attn_sched(p, f);
+        as_f = f;
+      }
       switch (k) {
-        case 0: gemv_dispatch(p, S, ring, GV_QKV, l, f, cta, in_id, tag, it, rb, gp); break;
-        case 1: attention_dispatch<HD>(p, S, ring, l, f, cta, tag, it, gp); break;
-        case 2: gemv_dispatch(p, S, ring, GV_O, l, f, cta, in_id, tag, it, rb, gp); break;
-        case 3: gemv_dispatch(p, S, ring, GV_GU, l, f, cta, in_id, tag, it, rb, gp); break;
-        default: gemv_dispatch(p, S, ring, GV_DOWN, l, f, cta, in_id, tag, it, rb, gp); break;
+        case 0: gemv_dispatch(p, S, ring, GV_QKV, l, f, cta, in_id, tag, rp, rb, gp); break;
+        case 1: attention_dispatch<HD>(p, S, ring, l, f, cta, tag, rp, gp, as); break;
+        case 2: gemv_dispatch(p, S, ring, GV_O, l, f, cta, in_id, tag, rp, rb, gp); break;
+        case 3: gemv_dispatch(p, S, ring, GV_GU, l, f, cta, in_id, tag, rp, rb, gp); break;
+        default: gemv_dispatch(p, S, ring, GV_DOWN, l, f, cta, in_id, tag, rp, rb, gp); break;
       }
     }
     trace_mark(p, gp, cta, 3);

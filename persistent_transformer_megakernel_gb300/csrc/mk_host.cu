@@ -25,12 +25,13 @@
 
 namespace {
 
-constexpr int kStageBytes = 32 * 1024;
+constexpr int kStageBytes = mk::STAGE_BYTES;
 constexpr int kMaxStagesWanted = 6;
 // split-KV: MAX_POLL_CHUNKS chunks up to MAX_POLL_CHUNKS * this many cached
 // positions, one chunk per this many beyond
 constexpr int kAttnPositionsPerChunk = 128;
-constexpr int kMinChunks = 64;   // split-KV chunk capacity per kv head (at least grid / Hkv)
+constexpr int kMinChunks = 64;
+   // split-KV chunk capacity per kv head (at least grid / Hkv)
 
 struct DeviceBuffers {
   std::vector<void *> owned;
@@ -78,9 +79,11 @@ int pow2_at_least(int v) {
 int make_geom(int K, int rows, bool pairs, mk::GemvGeom &g) {
   int kpt, tpr;
   if (choose_kpt(K, kpt, tpr) != MK_OK) return MK_ERR_UNSUPPORTED;
+  std::memset(&g, 0, sizeof(g));
   g.K = K;
   g.KPT = kpt;
   g.TPR = tpr;
+  g.BT = 1;
   g.NG = mk::NCT / tpr;
   const int rows_fit = kStageBytes / (K * 2);
   if (pairs) {
@@ -104,6 +107,74 @@ int make_geom(int K, int rows, bool pairs, mk::GemvGeom &g) {
   return MK_OK;
 }
 
+// The fast GEMV layouts compiled into the kernel (mk_device.cuh, gemv_dispatch):
+// {layout, KPT, rows per thread per tile, tiles per register batch}
+struct FastCase { int fast, kpt, rpt, bt; };
+const FastCase kFastCases[] = {{1, 32, 2, 4}, {1, 64, 1, 8}, {1, 16, 4, 2}, {1, 24, 2, 4}, {1, 8, 8, 1},
+                               {2, 8, 8, 1},  {2, 8, 8, 2},  {2, 12, 4, 2}, {2, 24, 2, 8}};
+
+// A fast layout for one GEMV phase, if one fits: the RMSNorm-fused phases
+// (QKV, gate/up, LM head) take the staged layout (one warp per row, the input
+// staged in shared memory), the O and down projections the split-K layout
+// (all consumer threads per row).  Returns false to keep the general layout.
+bool make_fast_geom(int kind, int K, int rows, int G, mk::GemvGeom &g) {
+  const bool normed = kind == mk::GV_QKV || kind == mk::GV_GU || kind == mk::GV_LM;
+  const bool pairs = kind == mk::GV_GU;
+  const int per_cta = (rows + G - 1) / G;
+  const FastCase *best = nullptr;
+  for (const FastCase &c : kFastCases) {
+    if (normed) {
+      if (c.fast != 1 || K != 32 * c.kpt || K > mk::MAX_STAGE_K) continue;
+      if (static_cast<long long>(mk::NCW) * c.rpt * K * 2 > kStageBytes) continue;   // 8 * RPT rows a tile
+      best = &c;
+      break;
+    }
+    if (c.fast != 2 || K != mk::NCT * c.kpt || c.kpt % 4) continue;
+    if (static_cast<long long>(c.rpt) * K * 2 > kStageBytes) continue;              // RPT rows a tile
+    // the fewest register slots that still hold every tile of a CTA, else the most
+    const int tiles = (per_cta + c.rpt - 1) / c.rpt;
+    if (!best) { best = &c; continue; }
+    const bool fits = tiles <= c.bt, best_fits = (per_cta + best->rpt - 1) / best->rpt <= best->bt;
+    if ((fits && (!best_fits || c.rpt * c.bt < best->rpt * best->bt)) ||
+        (!fits && !best_fits && c.rpt * c.bt > best->rpt * best->bt))
+      best = &c;
+  }
+  if (!best) return false;
+  g.K = K;
+  g.KPT = best->kpt;
+  g.fast = best->fast;
+  g.CH = (best->kpt % 8 == 0) ? 8 : 4;
+  g.BT = best->bt;
+  g.RPTP = best->rpt;
+  g.rows = rows;
+  if (best->fast == 1) {
+    g.TPR = 32;
+    g.NG = mk::NCW;
+    g.RT = pairs ? mk::NCW * best->rpt / 2 : mk::NCW * best->rpt;
+  } else {
+    g.TPR = mk::NCT;
+    g.NG = 1;
+    g.RT = best->rpt;
+  }
+  return true;
+}
+
+// log2 of v when v is a power of two, else -1
+int log2_exact(int v) {
+  if (v <= 0 || (v & (v - 1))) return -1;
+  int l = 0;
+  while ((1 << l) < v) ++l;
+  return l;
+}
+
+// the shift amounts the device code uses in place of divisions
+void fill_shifts(mk::GemvGeom &g) {
+  g.lgRT = log2_exact(g.RT);
+  g.invK = log2_exact(g.K) >= 0 ? 1.0f / static_cast<float>(g.K) : 0.0f;
+  g.lgCH = g.fast == 2 ? log2_exact(g.CH) : 0;
+  g.lgSpan = g.fast == 2 ? log2_exact(g.TPR * g.CH) : 0;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -116,7 +187,7 @@ struct mk_handle {
   int pos = 0;
   int max_chunks = 0;
   int stages = 0;
-  int ll_rep = 1;             // copies of every tagged buffer (MK_LL_REPLICAS); one measured fastest
+  int ll_rep = 1;             // copies of every tagged buffer; one measured fastest
   unsigned tag = 1;          // tag of the next forward's published activations
   size_t ll_words = 0;
   unsigned long long *ll_base = nullptr;
@@ -240,7 +311,7 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
     return MK_ERR_UNSUPPORTED;
   // the residual stream is stored in the input layout of its readers (next
   // layer's QKV and the LM head): both must split H the same way
-  if (geo[mk::GV_LM].KPT != geo[mk::GV_QKV].KPT || geo[mk::GV_LM].TPR != geo[mk::GV_QKV].TPR)
+  if (geo[mk::GV_LM].fast != geo[mk::GV_QKV].fast || geo[mk::GV_LM].KPT != geo[mk::GV_QKV].KPT || geo[mk::GV_LM].TPR != geo[mk::GV_QKV].TPR)
     return MK_ERR_UNSUPPORTED;
 
   mk_handle *h = new (std::nothrow) mk_handle();
@@ -260,6 +331,25 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
   if (!coop) return fail(MK_ERR_UNSUPPORTED);
   h->G = prop.multiProcessorCount;
   h->kernel = (d == 64) ? mk::kernel_d64() : mk::kernel_d128();
+  {
+    // fast layouts where one fits (the general ones above stay otherwise)
+    const int Ks[mk::GV_COUNT] = {H, Hq * d, H, I, H};
+    const int rows[mk::GV_COUNT] = {(Hq + 2 * Hkv) * d, H, I, H, c.vocab};
+    mk::GemvGeom fg[mk::GV_COUNT];
+    bool ok[mk::GV_COUNT];
+    for (int k = 0; k < mk::GV_COUNT; ++k) {
+      std::memset(&fg[k], 0, sizeof(fg[k]));
+      ok[k] = make_fast_geom(k, Ks[k], rows[k], h->G, fg[k]);
+    }
+    // the residual stream's layout is read by both the next layer's QKV and the
+    // LM head: either both take the staged layout or neither does
+    if (ok[mk::GV_QKV] != ok[mk::GV_LM]) ok[mk::GV_QKV] = ok[mk::GV_LM] = false;
+    for (int k = 0; k < mk::GV_COUNT; ++k) {
+      if (ok[k]) geo[k] = fg[k];
+      fill_shifts(geo[k]);
+      if (geo[k].fast == 2 && (geo[k].lgCH < 0 || geo[k].lgSpan < 0)) return fail(MK_ERR_UNSUPPORTED);
+    }
+  }
   // residual rows owned per CTA, and rows of every phase, must fit the static buffers
   if ((H + h->G - 1) / h->G > mk::MAX_OWN) return fail(MK_ERR_UNSUPPORTED);
   for (int k = 0; k < mk::GV_COUNT; ++k) {
@@ -281,13 +371,12 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
     return fail(MK_ERR_UNSUPPORTED);
   }
   h->max_chunks = std::max(kMinChunks, h->G / Hkv);
-  // tuning knobs: copies of the tagged activation buffers (readers pick copy
-  // cta % copies, spreading the broadcast reads over more L2 lines), poll back-off
-  if (const char *e = std::getenv("MK_LL_REPLICAS")) h->ll_rep = std::max(1, std::min(16, std::atoi(e)));
-  int poll_ns = 0;
-  if (const char *e = std::getenv("MK_POLL_SLEEP_NS")) poll_ns = std::max(0, std::min(10000, std::atoi(e)));
-  int attn_ppc = kAttnPositionsPerChunk;
-  if (const char *e = std::getenv("MK_ATTN_PPC")) attn_ppc = std::max(0, std::atoi(e));
+  // one copy of the tagged activation buffers (more copies, read by CTA index,
+  // measured slower: every producer then stores each word several times) and
+  // no back-off in the polls (any sleep measured slower)
+  h->ll_rep = 1;
+  const int poll_ns = 0;
+  const int attn_ppc = kAttnPositionsPerChunk;
 
   // ---- allocations ---------------------------------------------------------
   const int rope_len = c.rope_positions > 0 ? c.rope_positions : 2 * c.max_seq + 8;
@@ -442,8 +531,8 @@ int mk_decode_start(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t
   if (!d_out_ids || (n_in > 0 && !d_in_ids)) return MK_ERR_INVALID_ARG;
   mk_decode_opts o;
   std::memset(&o, 0, sizeof(o));
-  o.fault_skip_barrier = -1;
   if (opts) o = *opts;
+  if (o.fault_skip_barrier < 0) return MK_ERR_INVALID_ARG;
   if (o.n_embed_rows < 0 || o.attn_chunks < 0 || o.attn_chunks > h->max_chunks || o.spin_ns < 0 ||
       (o.flags & ~(MK_DECODE_PER_OP | MK_DECODE_PER_OP_GRAPH | MK_DECODE_STREAM)) ||
       (o.n_embed_rows > 0 && !o.embeds))
@@ -467,7 +556,7 @@ int mk_decode_start(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t
   p.trace = reinterpret_cast<unsigned long long *>(o.trace);
   p.chunks_override = o.attn_chunks;
   p.spin_ns = o.spin_ns > 0 ? o.spin_ns : 1000000000LL;
-  p.fault_barrier = o.fault_skip_barrier;
+  p.fault_barrier = o.fault_skip_barrier - 1;   // forward index, -1 = off
   if (o.codes) {
     p.cb_books = static_cast<const uint16_t *>(o.books);
     p.cb_text = static_cast<const uint16_t *>(o.text);

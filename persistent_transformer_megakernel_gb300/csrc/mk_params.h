@@ -24,6 +24,8 @@ constexpr int RED_ROWS = 64;         // rows of one GEMV epilogue batch
 constexpr int MAX_WPR = 8;           // warps that share one row (threads per row / 32)
 constexpr int MAX_GRP_HD = 256;      // group size * head_dim handled by one attention unit
 constexpr int MAX_POLL_CHUNKS = 8;    // split-KV chunk counts the chunk holding the new position merges by polling
+constexpr int MAX_STAGE_K = 2048;    // widest GEMV input staged in shared memory
+constexpr int STAGE_BYTES = 32 * 1024;   // one slot of the weight ring
 
 // GEMV phases in the order of their geometry table
 enum GemvKind { GV_QKV = 0, GV_O = 1, GV_GU = 2, GV_DOWN = 3, GV_LM = 4, GV_COUNT = 5 };
@@ -31,14 +33,34 @@ enum GemvKind { GV_QKV = 0, GV_O = 1, GV_GU = 2, GV_DOWN = 3, GV_LM = 4, GV_COUN
 // How a GEMV phase maps rows and the input width onto the consumer threads:
 // thread t owns KPT consecutive input elements (k-chunk t % TPR) of NG = NCT/TPR
 // row groups; a tile holds RT rows (GU: RT gate/up row pairs).
+//
+// Two layouts of a thread's slice exist.  The general one (fast == 0) gives
+// thread kc the KPT consecutive elements [kc*KPT, (kc+1)*KPT) and reduces one
+// tile at a time.  The fast ones give thread kc chunks of CH consecutive
+// elements, chunk c at c*TPR*CH + kc*CH (every shared-memory load of a warp
+// covers consecutive bytes), accumulate the row partials of BT tiles in
+// registers and reduce once per batch of tiles:
+//   fast == 1 (staged): TPR = 32, one warp per row; the CTA polls the input
+//             once into shared memory (natural order) and every warp reads
+//             the whole vector from there -- used for the RMSNorm-fused
+//             phases, whose norm needs the whole vector anyway;
+//   fast == 2 (split-K): TPR = 256, all consumer threads share each row; each
+//             thread polls its own slice directly (no CTA barrier before the
+//             tiles) -- used for the wide inputs of the O and down projections.
 struct GemvGeom {
   int K;        // input width
-  int KPT;      // input elements per thread (8, 12, 16, 24)
+  int KPT;      // input elements per thread
   int TPR;      // threads per row (32, 64, 128, 256)
   int NG;       // row groups = NCT / TPR
   int RT;       // rows (pairs for GU) per ring tile
-  int RPTP;     // rows per thread per tile, padded to a power of two (<= 16)
+  int RPTP;     // rows per thread per tile (general: padded to a power of two, <= 16)
   int rows;     // total rows (pairs for GU) of the phase
+  int fast;     // 0 general, 1 staged, 2 split-K (see above)
+  int CH;       // fast layouts: consecutive elements per chunk (4 or 8)
+  int BT;       // fast layouts: tiles per register batch
+  int lgCH, lgSpan;   // split-K layout: log2 of CH and of TPR * CH
+  int lgRT;     // log2 of RT when RT is a power of two, else -1
+  float invK;   // 1 / K when K is a power of two (exact), else 0 (divide)
 };
 
 struct LayerPtrs {
@@ -144,6 +166,7 @@ struct SmemCtl {
   float red[2][RED_ROWS][MAX_WPR];       // per-warp row partials of one epilogue batch
   float misc[64];
   float xown[MAX_OWN];                   // residual rows this CTA owns
+  int rr[GV_COUNT][2];                   // this CTA's row range of every GEMV phase
   int flags[F_COUNT];
   float bestv[NCW];
   int besti[NCW];
@@ -151,6 +174,7 @@ struct SmemCtl {
   float kcur[128], vcur[128];            // this position's key / value (bf16-rounded)
   float ow[NCW][MAX_GRP_HD];             // per-warp unnormalised attention outputs
   float mw[NCW][8], lw[NCW][8];          // per-warp running max / sum per head
+  alignas(16) float xs[MAX_STAGE_K];     // staged GEMV input (fast layout 1)
 };
 
 constexpr int RING_OFFSET = (int)((sizeof(SmemCtl) + 1023) / 1024 * 1024);
