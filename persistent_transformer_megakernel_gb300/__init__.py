@@ -10,6 +10,7 @@ from ._binding import (  # noqa: F401
     MKError,
     Decoder,
     embed_sum,
+    embed_sum_noalloc,
     error_string,
     lib_path,
     load_library,

@@ -174,6 +174,61 @@ def check_options(shape: dict, n: int, *, out=None, embeds=None, pos3=None, logi
             raise ValueError("talker tables must be [n_books][rows][H] and [rows][H], codes [rows][n_books]")
 
 
+def check_embed_sum(books, text, codes, text_ids, out, on_device: bool = True) -> None:
+    """Validate the tensors of ``mk_embed_sum`` / ``mk_embed_sum_noalloc``:
+    books bf16 [n_books][rows][H], text bf16 [rows][H], codes int32 [n][n_books],
+    text_ids int32 [n], out fp32 with at least n x H elements; all contiguous
+    (and on the device unless ``on_device`` is False).  Raises ValueError."""
+    if not isinstance(codes, torch.Tensor) or codes.dim() != 2:
+        raise ValueError("codes must be a [n][n_books] int32 tensor")
+    shape = dict(n_layers=0, hidden=books.shape[-1] if isinstance(books, torch.Tensor) and books.dim() == 3 else -1,
+                 vocab=0)
+    check_options(shape, codes.shape[0], talker=(books, text, codes, text_ids), on_device=on_device)
+    n, H = codes.shape[0], books.shape[2]
+    if not isinstance(out, torch.Tensor) or out.dtype != torch.float32 or not out.is_contiguous() or \
+            (on_device and not out.is_cuda) or out.numel() < n * H:
+        raise ValueError("out must be a contiguous fp32 %stensor of at least %d x %d elements"
+                         % ("device " if on_device else "", n, H))
+
+
+def check_weights(shape: dict, weights: dict, device=None) -> None:
+    """Every weight must have the shape the config implies (``[out][in]``
+    matrices, ``[n]`` gains); torch tensors must also be bf16, contiguous and
+    on ``device``; numpy arrays must be uint16 bf16 bit patterns.  Raises
+    ValueError (a wrong-sized matrix would otherwise be read past its end)."""
+    s = shape
+    H, L = s["hidden"], s["n_layers"]
+    d, Hq, Hkv, I = s["head_dim"], s["n_q_heads"], s["n_kv_heads"], s["intermediate"]
+    want = {"attn_norm": (H,), "wq": (Hq * d, H), "wk": (Hkv * d, H), "wv": (Hkv * d, H),
+            "q_norm": (d,), "k_norm": (d,), "wo": (H, Hq * d), "mlp_norm": (H,),
+            "w_gate": (I, H), "w_up": (I, H), "w_down": (H, I)}
+
+    def one(a, name, shp):
+        if isinstance(a, torch.Tensor):
+            if a.dtype != torch.bfloat16 or not a.is_contiguous() or \
+                    (device is not None and a.device != torch.device(device)):
+                raise ValueError("weight %s must be a contiguous bf16 tensor on %s" % (name, device))
+        elif isinstance(a, np.ndarray):
+            if a.dtype != np.uint16:
+                raise ValueError("weight %s must hold bf16 bit patterns (uint16)" % name)
+        else:
+            raise ValueError("weight %s must be a torch tensor or a numpy array" % name)
+        if tuple(a.shape) != tuple(shp):
+            raise ValueError("weight %s has shape %s; the config needs %s" % (name, tuple(a.shape), tuple(shp)))
+
+    one(weights["embed"], "embed", (s["vocab_in"], H))
+    one(weights["final_norm"], "final_norm", (H,))
+    if weights.get("lm_head") is not None:
+        one(weights["lm_head"], "lm_head", (s["vocab"], H))
+    elif s["vocab"] != s["vocab_in"]:
+        raise ValueError("a tied head needs vocab == vocab_in")
+    if len(weights["layers"]) != L:
+        raise ValueError("%d layers given; the config has %d" % (len(weights["layers"]), L))
+    for l, lw in enumerate(weights["layers"]):
+        for k, shp in want.items():
+            one(lw[k], "layers[%d].%s" % (l, k), shp)
+
+
 def _dev_bf16(bits: np.ndarray, device) -> torch.Tensor:
     t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
     return t.to(device, non_blocking=False).contiguous()
@@ -199,6 +254,7 @@ class Decoder:
         torch.cuda.set_device(self.device)
         self.shape = dict(shape)
         s = self.shape
+        check_weights(s, weights, self.device if isinstance(weights["embed"], torch.Tensor) else None)
         conv = (lambda a: a) if isinstance(weights["embed"], torch.Tensor) else \
             (lambda a: _dev_bf16(a, self.device))
         self._keep = []
@@ -291,7 +347,7 @@ class Decoder:
                per_op=False, embeds: Optional[torch.Tensor] = None,
                pos3: Optional[torch.Tensor] = None, logits: Optional[torch.Tensor] = None,
                hidden: Optional[torch.Tensor] = None, trace: Optional[torch.Tensor] = None,
-               attn_chunks: int = 0, spin_ns: int = 0, fault_skip_barrier: int = -1,
+               attn_chunks: int = 0, spin_ns: int = 0, fault_skip_barrier: int = 0,
                talker=None, stream=None) -> torch.Tensor:
         """``mk_decode``: ``in_ids`` (device int32 tensor, or a sequence moved to
         the device) then ``n_steps`` greedy forwards.  Returns the ids tensor.
@@ -335,7 +391,7 @@ class Decoder:
             out = torch.empty(max(n, 1), dtype=torch.int32, device=self.device)
         check_options(self.shape, n, out=out if all_ids else None, embeds=embeds, pos3=pos3, logits=logits,
                       hidden=hidden)
-        o = self._opts(False, embeds, pos3, logits, hidden, None, 0, 0, -1)
+        o = self._opts(False, embeds, pos3, logits, hidden, None, 0, 0, 0)
         _check(self.lib.mk_prefill(self.h, _ptr(d_in), n, _ptr(out) if all_ids else None, C.byref(o),
                                    _stream_ptr(stream)), "mk_prefill")
         return out[:n] if all_ids else None
@@ -358,7 +414,7 @@ class Decoder:
         if out is None:
             out = torch.empty(max(n, 1), dtype=torch.int32, device=self.device)
         check_options(self.shape, n, out=out, embeds=embeds, pos3=pos3)
-        o = self._opts(per_op, embeds, pos3, None, None, None, 0, 0, -1)
+        o = self._opts(per_op, embeds, pos3, None, None, None, 0, 0, 0)
         if stream_ids:
             o.flags |= MK_DECODE_STREAM
         self._pending_keep = (d_in, out, embeds, pos3)   # alive until the wait
@@ -413,7 +469,7 @@ class Decoder:
         n = ids.size + n_steps
         out = np.empty(max(n, 1), dtype=np.int32)
         check_options(self.shape, n, embeds=embeds, pos3=pos3)
-        o = self._opts(per_op, embeds, pos3, None, None, None, 0, 0, -1)
+        o = self._opts(per_op, embeds, pos3, None, None, None, 0, 0, 0)
         rc = self.lib.mk_decode_host(self.h, ids.ctypes.data_as(C.c_void_p) if ids.size else None,
                                      ids.size, n_steps, out.ctypes.data_as(C.c_void_p), C.byref(o),
                                      _stream_ptr(stream))
@@ -432,7 +488,23 @@ def embed_sum(books: torch.Tensor, text: torch.Tensor, codes: torch.Tensor, text
         out = torch.empty((n, H), dtype=torch.float32, device=books.device)
     codes_i = codes.to(torch.int32).contiguous()
     text_i = text_ids.to(torch.int32).contiguous()
+    check_embed_sum(books, text, codes_i, text_i, out)
     rc = lib.mk_embed_sum(_ptr(books), n_books, book_rows, _ptr(text), text.shape[0], H,
                           _ptr(codes_i), _ptr(text_i), n, _ptr(out), _stream_ptr(stream))
     _check(rc, "mk_embed_sum")
+    return out
+
+
+def embed_sum_noalloc(books: torch.Tensor, text: torch.Tensor, codes: torch.Tensor, text_ids: torch.Tensor,
+                      out: torch.Tensor, stream=None) -> torch.Tensor:
+    """``mk_embed_sum_noalloc``: the same rows as ``embed_sum`` into a caller
+    buffer, with the library's static scratch (at most 4096 rows a call); the
+    library allocates nothing.  ``out`` is required (fp32, >= n x H)."""
+    _require_cuda()
+    lib = load_library()
+    check_embed_sum(books, text, codes, text_ids, out)
+    n_books, book_rows, H = books.shape
+    rc = lib.mk_embed_sum_noalloc(_ptr(books), n_books, book_rows, _ptr(text), text.shape[0], H, _ptr(codes),
+                                  _ptr(text_ids), codes.shape[0], _ptr(out), _stream_ptr(stream))
+    _check(rc, "mk_embed_sum_noalloc")
     return out

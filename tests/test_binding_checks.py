@@ -58,3 +58,51 @@ def test_dtype_and_layout_are_checked():
     _bad(trace=_t(N, 11, G, 4, dtype=torch.int32), grid=G)
     with pytest.raises(ValueError):                # host tensors where device ones are needed
         check_options(S, N, out=_t(N, dtype=torch.int32))
+
+
+def test_embed_sum_tensors_are_checked():
+    from persistent_transformer_megakernel_gb300._binding import check_embed_sum
+    books, text = _t(16, 20, 8, dtype=torch.bfloat16), _t(30, 8, dtype=torch.bfloat16)
+    codes, tids = _t(N, 16, dtype=torch.int32), _t(N, dtype=torch.int32)
+    check_embed_sum(books, text, codes, tids, _t(N, 8), on_device=False)
+    check_embed_sum(books, text, codes, tids, _t(N * 8 + 3), on_device=False)   # larger out is fine
+    for bad in (_t(N - 1, 8), _t(N, 8, dtype=torch.float64), _t(8, N).t()):      # small, wrong dtype, strided
+        with pytest.raises(ValueError):
+            check_embed_sum(books, text, codes, tids, bad, on_device=False)
+    with pytest.raises(ValueError):                                            # fp32 tables
+        check_embed_sum(_t(16, 20, 8), text, codes, tids, _t(N, 8), on_device=False)
+    with pytest.raises(ValueError):                                            # codes per row != books
+        check_embed_sum(books, text, _t(N, 15, dtype=torch.int32), tids, _t(N, 8), on_device=False)
+    with pytest.raises(ValueError):                                            # host tensors
+        check_embed_sum(books, text, codes, tids, _t(N, 8))
+
+
+def test_weights_are_checked_against_the_config():
+    import numpy as np
+    from persistent_transformer_megakernel_gb300._binding import check_weights
+    s = dict(n_layers=1, hidden=8, n_q_heads=2, n_kv_heads=1, head_dim=4, intermediate=12, vocab=10, vocab_in=10)
+
+    def layer():
+        z = lambda *sh: np.zeros(sh, dtype=np.uint16)
+        return dict(attn_norm=z(8), wq=z(8, 8), wk=z(4, 8), wv=z(4, 8), q_norm=z(4), k_norm=z(4), wo=z(8, 8),
+                    mlp_norm=z(8), w_gate=z(12, 8), w_up=z(12, 8), w_down=z(8, 12))
+
+    good = dict(embed=np.zeros((10, 8), np.uint16), final_norm=np.zeros(8, np.uint16), lm_head=None,
+                layers=[layer()])
+    check_weights(s, good)
+    bad = dict(good, layers=[dict(layer(), wo=np.zeros((8, 4), np.uint16))])      # wrong width
+    with pytest.raises(ValueError):
+        check_weights(s, bad)
+    with pytest.raises(ValueError):                                               # transposed view
+        check_weights(s, dict(good, layers=[dict(layer(), w_down=np.zeros((12, 8), np.uint16))]))
+    with pytest.raises(ValueError):                                               # fp32 numbers
+        check_weights(s, dict(good, embed=np.zeros((10, 8), np.float32)))
+    with pytest.raises(ValueError):                                               # torch fp32 tensor
+        check_weights(s, dict(good, final_norm=torch.zeros(8)))
+    t = torch.zeros(8, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):                                               # non-contiguous bf16
+        check_weights(s, dict(good, layers=[dict(layer(), wq=t.t()[:, :8].t().contiguous().t())]))
+    with pytest.raises(ValueError):                                               # missing layer
+        check_weights(s, dict(good, layers=[]))
+    with pytest.raises(ValueError):                                               # untied head of wrong size
+        check_weights(s, dict(good, lm_head=np.zeros((9, 8), np.uint16)))
