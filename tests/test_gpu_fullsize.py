@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 mk = pytest.importorskip("persistent_transformer_megakernel_gb300")
 
 
-def _gpu_teacher_forced(dec, feed, embeds=None, pos3=None, hidden=True):
+def _gpu_teacher_forced(dec, feed, embeds=None, pos3=None, hidden=True, talker=None):
     s = dec.shape
     n = len(feed)
     logits = torch.full((n, s["vocab"]), float("nan"), dtype=torch.float32, device="cuda:0")
@@ -26,7 +26,7 @@ def _gpu_teacher_forced(dec, feed, embeds=None, pos3=None, hidden=True):
     if hidden:
         hid = torch.full((n, s["n_layers"] + 1, s["hidden"]), float("nan"), dtype=torch.float32,
                          device="cuda:0")
-    ids = dec.decode(feed, 0, logits=logits, hidden=hid, embeds=embeds, pos3=pos3)
+    ids = dec.decode(feed, 0, logits=logits, hidden=hid, embeds=embeds, pos3=pos3, talker=talker)
     torch.cuda.synchronize()
     return (ids.cpu().numpy(), logits.double().cpu().numpy(),
             None if hid is None else hid.double().cpu().numpy())
@@ -87,8 +87,19 @@ def test_tts_talker_sentinel_mrope_256():
     ref = O.Decoder(s, w, max_seq=n)
     ids_ref, lg_ref, hd_ref = ref.generate(sid, 0, sentinel_rows=E_ref, pos3=pos3)
     dec = mk.Decoder(s, w, max_seq=n)
-    ids, lg, hd = _gpu_teacher_forced(dec, sid, embeds=E, pos3=torch.as_tensor(pos3, device="cuda:0"))
+    p3 = torch.as_tensor(pos3, device="cuda:0")
+    ids, lg, hd = _gpu_teacher_forced(dec, sid, embeds=E, pos3=p3)
     _compare("tts_talker", s, ids, lg, hd, ids_ref, lg_ref, hd_ref)
+    # the same 256 forwards with the 17-way sum formed inside the decode kernel
+    # from the code rows (no precomputed buffer), against the same oracle run
+    books = torch.from_numpy(tables["codebooks"].view(np.int16)).view(torch.bfloat16).cuda()
+    txt = torch.from_numpy(tables["text"].view(np.int16)).view(torch.bfloat16).cuda()
+    talker = (books, txt, torch.as_tensor(codes, dtype=torch.int32).cuda().contiguous(),
+              torch.as_tensor(text, dtype=torch.int32).cuda().contiguous())
+    dec.reset()
+    ids_k, lg_k, hd_k = _gpu_teacher_forced(dec, sid, pos3=p3, talker=talker)
+    _compare("tts_talker in-kernel sum", s, ids_k, lg_k, hd_k, ids_ref, lg_ref, hd_ref)
+    assert np.array_equal(lg_k, lg) and np.array_equal(hd_k, hd)
     dec.close()
 
 

@@ -109,31 +109,55 @@ def test_sentinel_rows_from_gpu_embed_sum():
     assert_ids(ids, ids_ref, lg_ref)
 
 
-def test_per_op_path_is_bitwise_equal_to_persistent():
-    s = W.shape("mid")
+def _oracle_feed(name, n_prompt, n_steps, max_seq):
+    """The oracle's greedy run and the teacher-forced feed that replays it."""
+    s = W.shape(name)
     w = W.make_weights(s, seed=0)
-    prompt = W.make_prompt(s["vocab_in"], 6, seed=1)
+    prompt = W.make_prompt(s["vocab_in"], n_prompt, seed=1)
+    ids_ref, lg_ref, hd_ref = O.Decoder(s, w, max_seq=max_seq).generate(prompt, n_steps)
+    feed = np.concatenate([prompt, ids_ref[n_prompt - 1:n_prompt + n_steps - 1]]).astype(np.int32)
+    return s, w, prompt, feed, ids_ref, lg_ref, hd_ref
+
+
+def _assert_oracle(s, ids, lg, hd, ids_ref, lg_ref, hd_ref, what):
+    assert_close(lg, lg_ref, what + " logits")
+    for l in range(s["n_layers"] + 1):
+        assert_close(hd[:, l], hd_ref[:, l], "%s hidden[%d]" % (what, l))
+    assert_ids(ids, ids_ref, lg_ref, what + " ids")
+
+
+def test_per_op_path_matches_the_oracle_and_the_persistent_kernel():
+    # the launch-overhead ablation (one launch per phase): oracle parity on a
+    # teacher-forced run, and the same bits as the persistent kernel
+    s, w, prompt, feed, ids_ref, lg_ref, hd_ref = _oracle_feed("mid", 6, 10, 32)
     a = mk.Decoder(s, w, max_seq=32)
     b = mk.Decoder(s, w, max_seq=32)
-    ia, la, ha = _run_gpu(a, prompt, 10)
-    ib, lb, hb = _run_gpu(b, prompt, 10, per_op=True)
+    ia, la, ha = _run_gpu(a, feed)
+    ib, lb, hb = _run_gpu(b, feed, per_op=True)
+    _assert_oracle(s, ib, lb, hb, ids_ref, lg_ref, hd_ref, "per-op")
     assert np.array_equal(ia, ib) and np.array_equal(la, lb) and np.array_equal(ha, hb)
+    # free-running greedy through the per-op path, up to the oracle's first near tie
+    b.reset()
+    free = b.decode(prompt, 10, per_op=True).cpu().numpy()
+    k = first_near_tie(lg_ref)
+    assert np.array_equal(free[:k], ids_ref[:k])
 
 
-def test_per_op_graph_replay_is_bitwise_equal_to_persistent():
-    # the per-op ablation replayed from a captured graph of one forward: same
-    # math, call fields read from the device call block; two calls in a row
-    # reuse the graph at a new position
-    s = W.shape("mid")
-    w = W.make_weights(s, seed=0)
-    prompt = W.make_prompt(s["vocab_in"], 6, seed=1)
+def test_per_op_graph_replay_matches_the_oracle_and_the_persistent_kernel():
+    # the per-op ablation replayed from a captured graph of one forward: call
+    # fields read from the device call block; a second call reuses the graph
+    # at a new position.  Oracle parity on both calls (teacher-forced), and
+    # the same bits as the persistent kernel.
+    s, w, prompt, feed, ids_ref, lg_ref, hd_ref = _oracle_feed("mid", 6, 16, 40)
     a = mk.Decoder(s, w, max_seq=40)
     b = mk.Decoder(s, w, max_seq=40)
-    ia, la, ha = _run_gpu(a, prompt, 10)
-    ib, lb, hb = _run_gpu(b, prompt, 10, per_op="graph")
+    ia, la, ha = _run_gpu(a, feed[:16])
+    ib, lb, hb = _run_gpu(b, feed[:16], per_op="graph")
+    _assert_oracle(s, ib, lb, hb, ids_ref[:16], lg_ref[:16], hd_ref[:16], "graph replay")
     assert np.array_equal(ia, ib) and np.array_equal(la, lb) and np.array_equal(ha, hb)
-    ia2, la2, ha2 = _run_gpu(a, [], 6)
-    ib2, lb2, hb2 = _run_gpu(b, [], 6, per_op="graph")
+    ia2, la2, ha2 = _run_gpu(a, feed[16:])
+    ib2, lb2, hb2 = _run_gpu(b, feed[16:], per_op="graph")
+    _assert_oracle(s, ib2, lb2, hb2, ids_ref[16:], lg_ref[16:], hd_ref[16:], "graph replay, second call")
     assert np.array_equal(ia2, ib2) and np.array_equal(la2, lb2) and np.array_equal(ha2, hb2)
 
 
@@ -174,17 +198,22 @@ def test_in_kernel_talker_sum_equals_the_sentinel_buffer_path():
 
 def test_streaming_mailbox_publishes_every_id_while_the_launch_runs():
     # each greedy id reaches the host-mapped mailbox as soon as it is chosen:
-    # the stream equals the ids of a plain decode, and the first id is seen
-    # before the last one exists
+    # the stream equals the oracle's greedy ids up to its first near tie and
+    # the ids of a plain decode everywhere, and the first id is seen before
+    # the last one exists
     s = W.shape("mid")
     w = W.make_weights(s, seed=0)
     prompt = W.make_prompt(s["vocab_in"], 4, seed=1)
+    ids_orc, lg_orc, _ = O.Decoder(s, w, max_seq=256).generate(prompt, 200)
     ref = mk.Decoder(s, w, max_seq=256)
     ids_ref = ref.decode(prompt, 200).cpu().numpy()
     dec = mk.Decoder(s, w, max_seq=256)
     got = list(dec.decode_stream(prompt, 200))
     assert [g[0] for g in got] == list(range(204))
-    assert np.array_equal(np.array([g[1] for g in got]), ids_ref)
+    streamed = np.array([g[1] for g in got])
+    k = first_near_tie(lg_orc)
+    assert k > 0 and np.array_equal(streamed[:k], ids_orc[:k]), "stream differs from the oracle before forward %d" % k
+    assert np.array_equal(streamed, ids_ref)
     assert got[0][2] < got[-1][2]
     # the per-op path publishes the same stream
     dec.reset()
@@ -282,10 +311,11 @@ def test_errors_are_reported_not_raised_as_faults():
         dec.decode([1, 2, 3], 6)                                  # 9 forwards > max_seq 8
     assert e.value.code == -3
     dec.reset()
-    # a CTA that never arrives at the grid barrier closing forward 1: the
-    # others give up after the wait budget and the call returns a timeout
+    # a CTA that never arrives at the grid barrier closing forward 1 (hook
+    # value 2): the others give up after the wait budget and the call returns
+    # a timeout
     with pytest.raises(mk.MKError) as e:
-        dec.decode([1, 2], 1, spin_ns=20_000_000, fault_skip_barrier=1)
+        dec.decode([1, 2], 1, spin_ns=20_000_000, fault_skip_barrier=2)
     assert e.value.code == -5
     dec.reset()
     # forward counts whose sum does not fit an int32 are rejected before any
@@ -304,3 +334,28 @@ def test_errors_are_reported_not_raised_as_faults():
     assert dec.info()["position"] == 0
     ids = dec.decode([1, 2], 2)                                   # the handle still works
     assert ids.shape[0] == 4
+
+
+def test_zeroed_options_struct_is_a_plain_decode():
+    # a memset-zero mk_decode_opts (the natural C initialiser) must run a plain
+    # decode: every field's zero means "off" or "the default"
+    import ctypes as C
+    from persistent_transformer_megakernel_gb300 import _binding as B
+    s = W.shape("tiny")
+    w = W.make_weights(s, seed=0)
+    prompt = W.make_prompt(s["vocab_in"], 4, seed=1)
+    want = mk.Decoder(s, w, max_seq=16).decode(prompt, 4).cpu().numpy()
+    dec = mk.Decoder(s, w, max_seq=16)
+    d_in = torch.as_tensor(prompt, dtype=torch.int32, device="cuda:0")
+    d_out = torch.full((8,), -7, dtype=torch.int32, device="cuda:0")
+    st = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    o = B.mk_decode_opts()
+    C.memset(C.byref(o), 0, C.sizeof(o))
+    rc = dec.lib.mk_decode(dec.h, C.c_void_p(d_in.data_ptr()), 4, 4, C.c_void_p(d_out.data_ptr()), C.byref(o), st)
+    assert rc == 0, mk.error_string(rc)
+    assert np.array_equal(d_out.cpu().numpy(), want)
+    # a negative hook value is rejected on the host
+    o.fault_skip_barrier = -1
+    dec.reset()
+    assert dec.lib.mk_decode(dec.h, C.c_void_p(d_in.data_ptr()), 4, 0, C.c_void_p(d_out.data_ptr()),
+                             C.byref(o), st) == -1
