@@ -5,13 +5,19 @@
 //   warp 0     one lane issues the TMA loads of every K block (64 wide): the
 //              weight tile [128 x 64] and the three activation-term tiles
 //              [BN x 64], into a STAGES-deep shared-memory ring;
-//   warp 1     allocates the tensor-memory accumulator (128 lanes x BN fp32
-//              columns); one lane issues per K block 3 terms x 4 steps of
-//              tcgen05.mma (M 128, N BN, K 16), all into the one accumulator,
-//              and commits each stage back to the producer;
-//   warps 2-5  wait for the last commit, read the accumulator with
-//              tcgen05.ld (warp w owns TMEM lanes 32 (w % 4) ..) and store
-//              fp32 results, consecutive lanes writing consecutive n.
+//   warp 1     allocates three tensor-memory accumulators (128 lanes x BN
+//              fp32 columns each, one per activation term); one lane issues
+//              per K block 3 terms x 4 steps of tcgen05.mma (M 128, N BN,
+//              K 16) and commits each stage back to the producer;
+//   warps 2-5  wait for the last commit, read the accumulators with
+//              tcgen05.ld (warp w owns TMEM lanes 32 (w % 4) ..), add them
+//              (hi + mid) + lo and store fp32 results, consecutive lanes
+//              writing consecutive n.
+// Each term keeps its own accumulator because the tensor cores' fp32
+// accumulation is not round-to-nearest: summed into the large hi products at
+// every step, the small mid and lo products lost enough bits to triple the
+// 0.6B prompt's last-layer hidden-state error (0.030 against 0.009 with
+// separate accumulators, measured against the oracle).
 // Every wait is bounded (2 s); on expiry the CTA records MK_ERR_TIMEOUT,
 // still waits for the MMAs it issued, frees its tensor memory and returns.
 #include <cuda.h>
@@ -42,7 +48,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     pf_gemm(const __grid_constant__ WMaps wm, const __grid_constant__ CUtensorMap tx, const GemmCall c) {
   constexpr uint32_t B_BYTES = BN * 128;                 // one activation term: BN rows x 64 bf16
   constexpr uint32_t STAGE = A_BYTES + 3 * B_BYTES;
-  constexpr uint32_t TCOLS = BN < 32 ? 32 : BN;          // tensor-memory columns (a power of two)
+  constexpr uint32_t TCOLS = BN <= 32 ? 128 : BN <= 64 ? 256 : 512;   // 3 accumulators, a power of two
   constexpr uint32_t IDESC = idesc_bf16_f32(128, BN);
   extern __shared__ unsigned char smraw[];
   // 1024-byte alignment for the swizzled tiles
@@ -118,8 +124,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         for (int j = 0; j < 3; ++j)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_bf16(tbase, desc_sw128(sa + 32 * k), desc_sw128(sa + A_BYTES + j * B_BYTES + 32 * k), IDESC,
-                     (i | j | k) != 0);
+            mma_bf16(tbase + j * BN, desc_sw128(sa + 32 * k), desc_sw128(sa + A_BYTES + j * B_BYTES + 32 * k), IDESC,
+                     (i | k) != 0);
         mma_commit(&empty[s]);
       }
       // completes once every MMA issued above has finished (on the error path too)
@@ -137,8 +143,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll 1
       for (int cc = 0; cc < BN; cc += 16) {
         if (t0 + cc >= c.nt) break;                      // warp-uniform
-        float v[16];
+        float v[16], v1[16], v2[16];
         tmem_ld16(tbase + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(cc), v);
+        tmem_ld16(tbase + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(cc + BN), v1);
+        tmem_ld16(tbase + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(cc + 2 * BN), v2);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = (v[i] + v1[i]) + v2[i];
         if (r < nrows) {
 #pragma unroll
           for (int i = 0; i < 16; ++i)

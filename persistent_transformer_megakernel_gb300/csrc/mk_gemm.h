@@ -6,9 +6,10 @@
 // activation of token t enters as three bf16 terms hi, mid, lo (each the bf16
 // rounding of what the terms before it left, so hi + mid + lo holds fp32's 24
 // significant bits), stored as three bf16 matrices [tokens][K], one per term
-// (a 3-D tensor: K, token, term).  All three products accumulate into one fp32
-// accumulator in tensor memory (tcgen05.mma kind::f16, bf16 x bf16 -> fp32);
-// operands reach shared memory through 2-D TMA tensor loads.  K may be split
+// (a 3-D tensor: K, token, term).  Each term's products accumulate into its own
+// fp32 accumulator in tensor memory (tcgen05.mma kind::f16, bf16 x bf16 ->
+// fp32) and the three sums are added once at the end; operands reach shared
+// memory through TMA tensor loads.  K may be split
 // over `splits` CTAs per output tile; split s writes its own fp32 partial at
 // out + s * part_stride and the reader sums the partials in split order.
 #pragma once

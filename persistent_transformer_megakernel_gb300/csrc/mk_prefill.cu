@@ -3,10 +3,10 @@
 // tokens and run on the tensor cores (csrc/mk_gemm.cu: tcgen05.mma, bf16
 // operands staged by TMA, fp32 accumulators in tensor memory); every fp32
 // activation enters them as three bf16 terms (hi + mid + lo, 24 significant
-// bits, as many as fp32 holds) accumulated into one fp32 sum, so the products
-// lose nothing to the bf16 operand format.  The
-// rest -- RMSNorm, QK-norm, RoPE / MRoPE, the bf16 KV append, causal GQA
-// attention over the cache, residual adds, SiLU * up, greedy argmax -- are the
+// bits, as many as fp32 holds), each term's products in their own fp32
+// accumulator, so the products lose nothing to the bf16 operand format.  The
+// causal GQA attention runs on the tensor cores too (csrc/mk_pfattn.cu).  The
+// rest -- RMSNorm, QK-norm, RoPE / MRoPE, the bf16 KV append, attention over the cache, residual adds, SiLU * up, greedy argmax -- are the
 // kernels below.  The KV cache it fills is the decode kernel's, so decoding
 // continues from the prompt's last position (page A, "Porting a 1,200-line
 // persistent CUDA megakernel to Qwen3-TTS": time to first chunk is what the
@@ -641,8 +641,14 @@ int pf_enqueue(PfState &st, const PfArgs &a, const PfLayer *layers, const uint16
       if ((rc = project(st, wm[0], 0, rows, a.H, nt, 0, s_qkv, st.qkv_p, rows, a.qkv_stride, s))) break;
       const int jobs_warps = nt * (a.Hq + 2 * a.Hkv);
       const int wpb = PF_THREADS / 32;
-      if (a.d == 64) {
+      if (a.d == 64)
         pf_qk_rope_append<64><<<(jobs_warps + wpb - 1) / wpb, PF_THREADS, 0, s>>>(ac, l, w.q_norm, w.k_norm, t0, nt);
+      else
+        pf_qk_rope_append<128><<<(jobs_warps + wpb - 1) / wpb, PF_THREADS, 0, s>>>(ac, l, w.q_norm, w.k_norm, t0, nt);
+      if (st.kv_maps) {
+        // causal attention on the tensor cores
+        if ((rc = attn_tc_launch(st.kmap, st.vmap, ac, l, t0, nt, s))) break;
+      } else if (a.d == 64) {
         // groups mk_create accepts: group * head_dim <= 256
         switch (grp) {
           case 1: launch_attention<64, 1>(ac, l, t0, nt, s); break;
@@ -650,7 +656,6 @@ int pf_enqueue(PfState &st, const PfArgs &a, const PfLayer *layers, const uint16
           default: launch_attention<64, 4>(ac, l, t0, nt, s); break;
         }
       } else {
-        pf_qk_rope_append<128><<<(jobs_warps + wpb - 1) / wpb, PF_THREADS, 0, s>>>(ac, l, w.q_norm, w.k_norm, t0, nt);
         switch (grp) {
           case 1: launch_attention<128, 1>(ac, l, t0, nt, s); break;
           default: launch_attention<128, 2>(ac, l, t0, nt, s); break;
@@ -724,6 +729,7 @@ int pf_run(PfState &st, PfArgs a, const PfLayer *layers, const uint16_t *final_n
     if (!ok) return MK_ERR_CUDA;
     st.wmaps.swap(m);
   }
+  if (!st.kv_maps) st.kv_maps = attn_tc_maps(a, &st.kmap, &st.vmap);
   const int rows = (a.Hq + 2 * a.Hkv) * a.d;
   a.x = st.x; a.qkv = st.qkv; a.attn = st.attn;
   a.qkv_p = st.qkv_p; a.qkv_stride = T * rows;

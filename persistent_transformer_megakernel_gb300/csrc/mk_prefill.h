@@ -80,6 +80,9 @@ struct PfState {
   // then the LM head; the input terms per (K in H, Hq d, I) x (token block 32, 64, 128)
   std::vector<mkg::WMaps> wmaps;
   CUtensorMap xmaps[3][3];
+  // the KV cache as K and V tensors [L * Hkv * max_seq][d] for the tensor-core attention
+  CUtensorMap kmap, vmap;
+  bool kv_maps = false;
   struct Graph {
     int n;
     bool all_logits;
@@ -92,6 +95,12 @@ struct PfState {
 };
 
 int pf_init(PfState &st, int tc, int H, int Hq, int Hkv, int d, int I);
+
+// Tensor-core causal attention of a chunk (csrc/mk_pfattn.cu): the maps of the
+// KV cache (made once per handle), and one launch per layer and chunk.
+bool attn_tc_maps(const PfArgs &a, CUtensorMap *tk, CUtensorMap *tv);
+int attn_tc_launch(const CUtensorMap &tk, const CUtensorMap &tv, const PfArgs &a, int layer, int t0, int nt,
+                   cudaStream_t s);
 void pf_free(PfState &st);
 
 // Run n prompt forwards (positions call.pos0 ..): fills the KV cache, writes
