@@ -626,8 +626,10 @@ __device__ __noinline__ void gemv_phase(const Params &p, SmemCtl &S, unsigned ch
 // ---------------------------------------------------------------------------
 // dot of one bf16 row in shared memory with the thread's slice in the chunked
 // layout: chunk c of thread kc holds the CH elements from c*SPAN + kc*CH, so
-// every load of a warp covers consecutive bytes.  One accumulator per chunk,
-// summed in chunk order.
+// every load of a warp covers consecutive bytes.  One accumulator per chunk;
+// the chunk sums combine pairwise (a shallower tree than a running sum: the
+// rounding error of long per-lane sums shows up at the 1.7B shape's fp32 noise
+// floor).
 template <int KPT, int CH, int SPAN>
 __device__ __forceinline__ float dot_chunked(const unsigned char *row, int kc, const float (&xr)[KPT]) {
   constexpr int NCH = KPT / CH;
@@ -655,9 +657,17 @@ __device__ __forceinline__ float dot_chunked(const unsigned char *row, int kc, c
     }
     s[c] = a;
   }
-  float r = s[0];
+  float r;
+  if constexpr (NCH == 8) r = ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
+  else if constexpr (NCH == 4) r = (s[0] + s[1]) + (s[2] + s[3]);
+  else if constexpr (NCH == 3) r = (s[0] + s[1]) + s[2];
+  else if constexpr (NCH == 2) r = s[0] + s[1];
+  else {
+    static_assert(NCH == 1 || NCH == 6, "chunk counts of the compiled layouts");
+    r = s[0];
 #pragma unroll
-  for (int c = 1; c < NCH; ++c) r += s[c];
+    for (int c = 1; c < NCH; ++c) r += s[c];
+  }
   return r;
 }
 
@@ -937,10 +947,11 @@ __device__ __forceinline__ AttnSched attn_sched(const Params &p, int f) {
   a.P = p.pos0 + f;
   a.ctx = a.P + 1;
   int cmax = p.chunks_override > 0 ? p.chunks_override : max(1, p.G / p.Hkv);
-  // up to poll_cm * attn_ppc positions: poll_cm chunks (merged by polling);
-  // longer contexts: one chunk per attn_ppc positions (ticket merge)
+  // up to attn_min_chunks * attn_ppc positions: attn_min_chunks chunks; longer
+  // contexts: one chunk per attn_ppc positions (up to poll_cm chunks merge by
+  // polling, more by the last-arriving CTA)
   if (p.chunks_override <= 0 && p.attn_ppc > 0)
-    cmax = min(cmax, max((a.ctx + p.attn_ppc - 1) / p.attn_ppc, min(p.poll_cm, a.ctx)));
+    cmax = min(cmax, max((a.ctx + p.attn_ppc - 1) / p.attn_ppc, min(p.attn_min_chunks, a.ctx)));
   cmax = min(cmax, p.max_chunks);
   a.cs = (a.ctx + cmax - 1) / cmax;
   a.C = (a.ctx + a.cs - 1) / a.cs;
@@ -1389,44 +1400,6 @@ struct Producer {
     }
   }
 
-  // Prefetch this CTA's weight rows of a later GEMV phase into L2 (at most
-  // PREFETCH_MAX bytes per matrix range), so that its ring fills come from L2
-  // rather than from HBM: the ring alone holds only a few tiles ahead.
-  static constexpr uint32_t PREFETCH_MAX = 256 * 1024;
-  __device__ void prefetch_range(const uint16_t *src, uint32_t bytes) {
-    bulk_prefetch_l2(src, bytes < PREFETCH_MAX ? bytes : PREFETCH_MAX);
-  }
-  __device__ void prefetch_phase(int kind, int layer) {
-    const GemvGeom &g = p.geo[kind];
-    const int r0 = S.rr[kind][0], r1 = S.rr[kind][1];
-    if (r1 <= r0) return;
-    const uint32_t rowb = static_cast<uint32_t>(g.K) * 2u;
-    const LayerPtrs &L = S.layers[layer];
-    if (kind == GV_QKV) {
-      const int qr = p.Hq * p.d, kr = p.Hkv * p.d;
-      const int segs[4] = {0, qr, qr + kr, qr + 2 * kr};
-      const uint16_t *mats[3] = {L.wq, L.wk, L.wv};
-#pragma unroll
-      for (int s = 0; s < 3; ++s) {
-        const int lo = max(r0, segs[s]), hi = min(r1, segs[s + 1]);
-        if (lo < hi) prefetch_range(mats[s] + static_cast<size_t>(lo - segs[s]) * g.K, (hi - lo) * rowb);
-      }
-    } else if (kind == GV_GU) {
-      prefetch_range(L.w_gate + static_cast<size_t>(r0) * g.K, (r1 - r0) * rowb);
-      prefetch_range(L.w_up + static_cast<size_t>(r0) * g.K, (r1 - r0) * rowb);
-    } else {
-      const uint16_t *base = kind == GV_O ? L.wo : kind == GV_DOWN ? L.w_down : p.lm_head;
-      prefetch_range(base + static_cast<size_t>(r0) * g.K, (r1 - r0) * rowb);
-    }
-  }
-  // the GEMV phase ph of a forward (attention phases have no weights: -1)
-  __device__ void prefetch_ph(int ph) {
-    if (ph == 5 * p.L) { prefetch_phase(GV_LM, 0); return; }
-    const int l = ph / 5, k = ph - 5 * l;
-    if (k == 1) return;
-    prefetch_phase(k == 0 ? GV_QKV : k == 2 ? GV_O : k == 3 ? GV_GU : GV_DOWN, l);
-  }
-
   template <int HD>
   __device__ void kv_tiles(int l, int f, int cta) {
     if (as_f != f) {
@@ -1589,16 +1562,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
     if (lane == 0) {
       Producer pr(p, S, ring);
       int f = f0, ph = ph0;
-      // weights of the phases PF_AHEAD ahead are prefetched into L2 (persistent path)
-      constexpr int PF_AHEAD = 2;
-      if (!p.per_op)
-        for (int a = 0; a < PF_AHEAD && gp_begin + a < gp_end; ++a) pr.prefetch_ph((ph0 + a) % NPH);
       for (int gp = gp_begin; gp < gp_end && !pr.stop; ++gp) {
-        if (!p.per_op && gp + PF_AHEAD < gp_end) {
-          int pa = ph + PF_AHEAD;
-          if (pa >= NPH) pa -= NPH;
-          pr.prefetch_ph(pa);
-        }
         if (ph == 5 * p.L) {
           pr.gemv_tiles(GV_LM, 0, cta);
         } else {

@@ -2,9 +2,10 @@
 //
 // mk_create validates the shape, fixes the GEMV thread geometry of every phase,
 // allocates the KV cache and scratch, builds the rotary cos/sin table on the
-// host in double precision ("RoPE freq? Python tables only", page B = "I made a
-// single CUDA kernel speak: streaming Qwen3-TTS at 50ms latency on an RTX 5090",
-// section "So, What's the Catch with These Megakernels?") and checks that one
+// host in double precision (page B = "I made a single CUDA kernel speak:
+// streaming Qwen3-TTS at 50ms latency on an RTX 5090", section "So, What's the
+// Catch with These Megakernels?": the rotary frequencies are host-built tables)
+// and checks that one
 // CTA per SM fits.  mk_decode runs all forwards of a call in one cooperative
 // launch (page A = "Porting a 1,200-line persistent CUDA megakernel to
 // Qwen3-TTS", section "The idea: one kernel that never exits"), or, with
@@ -29,7 +30,10 @@ constexpr int kStageBytes = mk::STAGE_BYTES;
 constexpr int kMaxStagesWanted = 6;
 // split-KV: MAX_POLL_CHUNKS chunks up to MAX_POLL_CHUNKS * this many cached
 // positions, one chunk per this many beyond
-constexpr int kAttnPositionsPerChunk = 128;
+constexpr int kAttnPositionsPerChunk = 256;
+// split-KV chunks of a short context (measured on the 0.6B shape at 33..160
+// cached positions: 2/3/4/5/6/8 chunks gave 679/670/668/671/677/683 us/token)
+constexpr int kShortContextChunks = 4;
 constexpr int kMinChunks = 64;
    // split-KV chunk capacity per kv head (at least grid / Hkv)
 
@@ -472,6 +476,7 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
   p.poll_ns = poll_ns;
   p.attn_ppc = attn_ppc;
   p.poll_cm = mk::MAX_POLL_CHUNKS;
+  p.attn_min_chunks = kShortContextChunks;
   p.part = part;
   p.cand_val = cand_val; p.cand_idx = cand_idx; p.tickets = tickets;
   p.bar = reinterpret_cast<unsigned *>(h->d_sync);

@@ -144,6 +144,7 @@ struct Params {
   int chunks_override;
   int poll_cm;                     // chunk counts in (1, poll_cm] merge by polling; more: ticket merge
   int attn_ppc;                    // target cached positions per split-KV chunk (0: one chunk per CTA share)
+  int attn_min_chunks;             // chunks of a short context (fewer than attn_ppc positions each)
   long long spin_ns;
   int fault_barrier;
   int G;                           // CTAs

@@ -61,11 +61,6 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
-// start moving [src, src + bytes) from memory into L2 (no destination, no
-// completion to wait for); src 16-byte aligned, bytes a multiple of 16
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 // make this thread's view of generic-proxy global writes visible to later
 // async-proxy (bulk copy) reads, and the other way round
 __device__ __forceinline__ void fence_proxy_async_global() {
