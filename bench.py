@@ -150,28 +150,35 @@ class ClockSampler:
 # CPU oracle timing (the reported baseline / the reference arm)
 # ---------------------------------------------------------------------------
 def cpu_oracle_rate(workload: str, n_forwards: int, threads: int, warmup: int = 0, steps: int = 1):
-    """Time the oracle in a child process with a fixed BLAS thread count: build
-    it once, run ``warmup`` untimed then ``steps`` timed samples of
-    ``n_forwards`` teacher-forced forwards.  Returns the seconds per sample."""
+    """Time the oracle in a child process with a fixed BLAS thread count, at
+    the contexts the GPU times: the workload's prompt is laid into the cache
+    by the oracle's all-positions path (untimed), then ``warmup`` untimed and
+    ``steps`` timed samples of ``n_forwards`` teacher-forced forwards follow
+    it.  Returns (seconds per timed sample, first and last context timed)."""
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = str(threads)
     code = (
         "import sys,time,json; sys.path.insert(0, %r)\n"
-        "import workloads as W, oracle as O\n"
+        "import numpy as np, workloads as W, oracle as O\n"
         "wl=W.WORKLOADS[%r]; s=W.shape(wl['shape']); w=W.make_weights(s, seed=0)\n"
-        "Wt=O.decoder.Weights(O.DecoderShape.from_dict(s), w); del w\n"
-        "n=%d; reps=%d+%d\n"
-        "dec=O.Decoder(s, None, max_seq=n*reps+2, weights=Wt)\n"
-        "p=W.make_prompt(s['vocab_in'], n*reps+1, seed=1)\n"
-        "dec.generate(p[:1], 0); out=[]\n"
+        "shp=O.DecoderShape.from_dict(s); Wt=O.decoder.Weights(shp, w); del w\n"
+        "n=%d; reps=%d+%d; P0=max(1, wl['prompt'])\n"
+        "dec=O.Decoder(shp, None, max_seq=P0+n*reps+2, weights=Wt)\n"
+        "p=W.make_prompt(s['vocab_in'], P0+n*reps, seed=1)\n"
+        "_, _, K, V = O.prefix_forward(shp, None, p[:P0], logits_for=[P0-1], weights=Wt)\n"
+        "dec.K[:, :, :P0]=K; dec.V[:, :, :P0]=V; dec.pos=P0; del K, V\n"
+        "out=[]\n"
         "for r in range(reps):\n"
-        "    t=time.perf_counter(); dec.generate(p[1+r*n:1+(r+1)*n], 0); out.append(time.perf_counter()-t)\n"
-        "print(json.dumps(out[%d:]))\n" % (ROOT, workload, n_forwards, warmup, steps, warmup))
+        "    t=time.perf_counter(); dec.generate(p[P0+r*n:P0+(r+1)*n], 0); out.append(time.perf_counter()-t)\n"
+        "first=P0+%d*n+1\n"
+        "print(json.dumps([out[%d:], first, P0+n*reps]))\n" % (ROOT, workload, n_forwards, warmup, steps,
+                                                               warmup, warmup))
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("oracle timing failed: " + r.stderr[-2000:])
-    return json.loads(r.stdout.strip().splitlines()[-1])
+    dts, c0, c1 = json.loads(r.stdout.strip().splitlines()[-1])
+    return dts, (c0, c1)
 
 
 def reduce_timing(total_ms, units_per_rank, world, device="cpu"):
@@ -205,7 +212,7 @@ def run_reference(args, rank, world):
         return
     threads = cpu_threads()
     n = max(1, args.cpu_forwards)
-    dts = cpu_oracle_rate(args.workload, n, threads, warmup=1, steps=args.steps)
+    dts, ctx = cpu_oracle_rate(args.workload, n, threads, warmup=1, steps=args.steps)
     total = sum(dts)
     value = n * len(dts) / total
     line = {
@@ -216,11 +223,63 @@ def run_reference(args, rank, world):
         "data": "synthetic (seeded random-init weights, random prompt ids)",
         "config": {"workload": desc},
         "cpu_baseline": {"value": value, "unit": "tok/s", "cores": threads, "kind": "oracle",
-                         "sample": "%d teacher-forced forwards per step at context 2..%d, "
-                                   "float64 numpy oracle, BLAS threads %d" % (n, n * (args.steps + 1) + 1, threads)},
+                         "sample": "%d teacher-forced forwards per step at contexts %d..%d (after the "
+                                   "workload's prompt), float64 numpy oracle, BLAS threads %d"
+                                   % (n, ctx[0], ctx[1], threads)},
         "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def talker_ttfc(dev, n_prompt=32, chunk=16, reps=4):
+    """Time to first chunk on the talker workload (28 layers, hidden 1024,
+    3072-entry untied head, MRoPE): host code ids in -> the prompt's 17-way
+    input sums (mk_embed_sum) -> the prompt through mk_prefill (sentinel rows,
+    three distinct MRoPE position streams) -> greedy forwards streamed through
+    the host-mapped mailbox.  Host wall clock from the host ids to the first
+    generated id and to the first ``chunk`` ids on the host; best of the reps
+    after the first (which allocates the prefill scratch and captures it)."""
+    import torch
+    import persistent_transformer_megakernel_gb300 as mk
+    s = W.shape("tts_talker")
+    w = W.make_weights(s, seed=0)
+    dec = mk.Decoder(s, w, max_seq=n_prompt + chunk + 8, device=dev)
+    del w
+    tables = W.make_tts_tables(s["hidden"], seed=3)
+    books = torch.from_numpy(tables["codebooks"].view(np.int16)).view(torch.bfloat16).to(dev)
+    txt = torch.from_numpy(tables["text"].view(np.int16)).view(torch.bfloat16).to(dev)
+    del tables
+    codes, text = W.make_tts_codes(n_prompt, seed=2)
+    h_codes = torch.as_tensor(codes, dtype=torch.int32).pin_memory()
+    h_text = torch.as_tensor(text, dtype=torch.int32).pin_memory()
+    h_pos3 = torch.as_tensor(W.make_pos3(0, n_prompt, distinct=True), dtype=torch.int32).pin_memory()
+    sid = torch.as_tensor(W.sentinel_ids(n_prompt), dtype=torch.int32).pin_memory()
+    first, first_chunk = [], []
+    for _ in range(reps):
+        dec.reset()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        c_d = h_codes.to(dev, non_blocking=True)
+        t_d = h_text.to(dev, non_blocking=True)
+        E = mk.embed_sum(books, txt, c_d, t_d)
+        dec.prefill(sid.to(dev, non_blocking=True), all_ids=False, embeds=E,
+                    pos3=h_pos3.to(dev, non_blocking=True))
+        t_first = t_chunk = None
+        for i, _tok, _t in dec.decode_stream(None, chunk):
+            now = time.perf_counter() - t0
+            if t_first is None:
+                t_first = now
+            if i == chunk - 1:
+                t_chunk = now
+        first.append(t_first * 1e3)
+        first_chunk.append(t_chunk * 1e3)
+    dec.close()
+    return {"ttfc_talker_ms": min(first_chunk[1:]), "first_id_talker_ms": min(first[1:]),
+            "chunk_ids": chunk, "prompt_rows": n_prompt,
+            "talker_note": "talker shape (0.6B dims, 3072-entry head, MRoPE 24/20/20): host code ids -> mk_embed_sum -> "
+                    "mk_prefill of %d sentinel rows -> MK_DECODE_STREAM greedy forwards; host wall clock to the "
+                    "first id and to the first %d ids in the mailbox, best of %d after a first call"
+                    % (n_prompt, chunk, reps - 1)}
 
 
 def run_gpu(args, rank, world):
@@ -234,16 +293,20 @@ def run_gpu(args, rank, world):
     n_prompt, n_steps = wl["prompt"], wl["steps"]
     sentinel = wl.get("sentinel", False)
 
-    # CPU baseline before any heavy GPU work (rank 0 at N=1 only)
+    # CPU baseline before any heavy GPU work (rank 0 at N=1 only): the oracle at
+    # one thread and at every host thread, over forwards at the timed contexts
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         threads = cpu_threads()
         n_cpu = max(1, args.cpu_forwards)
-        dts = cpu_oracle_rate(args.workload, n_cpu, threads, warmup=0, steps=1)
+        dts, ctx = cpu_oracle_rate(args.workload, n_cpu, threads, warmup=0, steps=1)
+        dts1, _ = cpu_oracle_rate(args.workload, n_cpu, 1, warmup=0, steps=1)
         rate = n_cpu / dts[0]
         cpu = {"value": rate, "unit": "tok/s", "cores": threads, "kind": "oracle",
-               "sample": "%d teacher-forced forwards of the same model at context 2..%d, "
-                         "float64 numpy oracle, BLAS threads %d" % (n_cpu, n_cpu + 1, threads)}
+               "single_thread": {"value": n_cpu / dts1[0], "unit": "tok/s", "cores": 1},
+               "sample": "%d teacher-forced forwards of the same model at contexts %d..%d (after the "
+                         "workload's prompt, laid in by the oracle's all-positions path), float64 numpy "
+                         "oracle; value at %d BLAS threads, single_thread at 1" % (n_cpu, ctx[0], ctx[1], threads)}
 
     w = W.make_weights(s, seed=0)
     max_seq = n_prompt + n_steps + 8
@@ -381,7 +444,12 @@ def run_gpu(args, rank, world):
                                  "same prompt through mk_prefill (batched tensor-core GEMMs), best of 3 after "
                                  "a first call that allocates the scratch" % len(host_prompt)}
 
-    # launch-overhead ablation: the same phases as one ordinary launch each
+    if streaming is not None:
+        streaming.update(talker_ttfc(dev))
+
+    # launch-overhead ablation: the same phases as one ordinary launch each,
+    # i.e. this megakernel relaunched once per phase (its prologue repeats
+    # every launch), not a path of separate slim per-op kernels
     ablation = None
     if not args.no_ablation:
         n_ab = min(args.ablation_forwards, n_timed)
@@ -419,6 +487,8 @@ def run_gpu(args, rank, world):
             if timed:
                 g_ms = e0.elapsed_time(e1)
         ablation = {"us_per_token": ab_ms * 1e3 / n_ab, "forwards": n_ab,
+                    "what": "the persistent kernel's phases, one ordinary launch per phase (the megakernel "
+                            "relaunched with one phase each), then the same launches replayed from a graph",
                     "launches_per_forward": 5 * s["n_layers"] + 1,
                     "graph_replay_us_per_token": g_ms * 1e3 / n_ab,
                     "persistent_us_per_token": total_ms * 1e3 / (n_timed * args.steps)}

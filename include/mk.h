@@ -3,8 +3,9 @@
  *
  * Batch-1 autoregressive decode of a Qwen3-style decoder run as ONE
  * cooperatively launched kernel that loops over layers and decode steps
- * without exiting ("launch one kernel that owns the GPU and loops over decode
- * steps internally", page A section "The idea: one kernel that never exits").
+ * without exiting (page A, section "The idea: one kernel that never exits":
+ * a single resident kernel that takes the whole GPU and runs the decode loop
+ * itself instead of a chain of per-op launches).
  * Around that loop: a batched prompt prefill on tensor cores (mk_prefill), a
  * streaming mailbox the kernel fills with each greedy id while it runs
  * (mk_decode_start / mk_mailbox_read), and the per-op ablation of the same
@@ -54,8 +55,8 @@ typedef void *mk_stream; /* cudaStream_t */
 
 /* ---- model description ---------------------------------------------------
  * Qwen3-style decoder (page B, "Why Does a Single Kernel Even Matter for
- * TTS?": the TTS talker "mirrors Qwen3-0.6B exactly -- same dims, layers,
- * heads"; vocab, RoPE frequencies and the untied head differ).  The page's
+ * TTS?": the TTS talker has the dimensions, layer count and heads of
+ * Qwen3-0.6B; vocab, RoPE frequencies and the untied head differ).  The page's
  * kernel bakes these into compile-time constants (page A, "Porting it to
  * Qwen3-TTS-1.7B"); here they are runtime fields checked at mk_create, with
  * head_dim a template parameter of the kernel.
@@ -78,15 +79,17 @@ typedef struct {
   float rms_eps;           /* RMSNorm epsilon inside the root (Qwen3: 1e-6) */
   float rope_theta;        /* rotary base (Qwen3: 1e6) */
   int32_t rope_mode;       /* 0 = RoPE, 1 = sectioned MRoPE (page A, "Porting it to
-                              Qwen3-TTS-1.7B": "splits position encoding into sections"):
-                              contiguous runs of pairs per stream; 2 = interleaved MRoPE:
+                              Qwen3-TTS-1.7B": the talker's rotary positions come in
+                              sections, one position stream each): contiguous runs of
+                              pairs per stream; 2 = interleaved MRoPE:
                               pair i with i % 3 = s in {1, 2} follows stream s while
                               i < 3 * mrope_sections[s], every other pair stream 0 */
   int32_t mrope_sections[3]; /* rotary pairs driven by position streams 0, 1, 2 */
   int32_t max_seq;         /* KV-cache capacity in positions */
   int32_t rope_positions;  /* rows of the host-built cos/sin table; 0 = 2*max_seq + 8
-                              ("RoPE freq? Python tables only", page B, "So, What's
-                              the Catch with These Megakernels?") */
+                              (page B, "So, What's the Catch with These Megakernels?":
+                              the rotary frequencies come from tables the host
+                              builds, not from the kernel) */
   uint32_t flags;          /* reserved, must be 0 */
 } mk_config;
 
@@ -111,8 +114,10 @@ typedef struct {
 
 /* ---- per-call options (all optional; pass NULL for defaults) ------------ */
 #define MK_DECODE_PER_OP 1u  /* run the same math as one ordinary kernel launch per
-                                phase (the launch-overhead ablation; page A, "The idea":
-                                a conventional step "launches a long chain of kernels") */
+                                phase: this kernel relaunched once per phase (the
+                                launch-overhead ablation; page A, "The idea: one kernel
+                                that never exits": a conventional decode step is a long
+                                chain of separate kernel launches) */
 #define MK_DECODE_STREAM 4u    /* publish each forward's greedy id to the handle's
                                 host-mapped mailbox the moment it is chosen, so the
                                 host can consume ids while the launch still runs
@@ -128,8 +133,9 @@ typedef struct {
   uint32_t flags;             /* MK_DECODE_* bits */
   const float *embeds;        /* device [n_embed_rows][H] fp32 precomputed input rows;
                                  id -(r+1) selects row r (page B, "Why Does a Single
-                                 Kernel Even Matter for TTS?": "If token_id >=0, lookup
-                                 embedding. Else, grab precomputed from buffer") */
+                                 Kernel Even Matter for TTS?": a non-negative id is
+                                 looked up, any other input comes precomputed from a
+                                 buffer) */
   int32_t n_embed_rows;
   const int32_t *pos3;        /* device [3][n_in + n_steps] position streams for MRoPE;
                                  NULL = the slot index in every stream */
@@ -142,8 +148,9 @@ typedef struct {
                                  phase: after the grid barrier that closes the forward);
                                  or NULL */
   int32_t attn_chunks;        /* split-KV chunks per kv head; 0 = the library's policy
-                                 (8 chunks merged by polling up to 1024 cached positions,
-                                 then one chunk per 128 positions up to grid / n_kv_heads) */
+                                 (4 chunks up to 1024 cached positions, then one chunk
+                                 per 256 positions up to grid / n_kv_heads; up to 8
+                                 chunks merge by polling, more by the last CTA) */
   int64_t spin_ns;            /* budget of every device wait; 0 = 1 s */
   int32_t fault_skip_barrier; /* test hook: N > 0 makes CTA 0 skip its arrival at the
                                  grid barrier that closes forward N - 1 (persistent path
@@ -155,8 +162,8 @@ typedef struct {
      accumulated in fp32 in table order (codebook 0 .. n_books-1, then text) --
      the same sum mk_embed_sum writes, so the result is bitwise that of the
      embeds path fed by mk_embed_sum (page B, "Why Does a Single Kernel Even
-     Matter for TTS?": inputs "are sums of 17 embeddings (16 codebooks +
-     text)").  codes and embeds are exclusive.  A code or text id out of range
+     Matter for TTS?": each talker input is the 17-way codebook + text sum).
+     codes and embeds are exclusive.  A code or text id out of range
      gives MK_ERR_BAD_TOKEN. */
   const void *books;          /* device bf16 [n_books][book_rows][H] */
   int32_t n_books;            /* 0 .. 64 */
@@ -183,12 +190,20 @@ typedef struct {
 /* Validate cfg, allocate the KV cache [L][Hkv][max_seq][d] bf16 (keys and
  * values), scratch, barrier/error words and the cos/sin table (built on the
  * host in double precision), and check that one CTA per SM fits.  *out gets
- * the handle.  Errors: MK_ERR_INVALID_ARG, MK_ERR_UNSUPPORTED, MK_ERR_NO_MEMORY,
- * MK_ERR_CUDA (nothing is leaked on failure). */
+ * the handle.  The pages fix no interface beyond the model constants and the
+ * token-id-or-buffer input (page A, "Porting it to Qwen3-TTS-1.7B"; page B,
+ * "Why Does a Single Kernel Even Matter for TTS?"); the handle holds what the
+ * persistent kernel keeps between calls (page A, "The idea: one kernel that
+ * never exits": the KV cache and the step loop's state).  Errors:
+ * MK_ERR_INVALID_ARG, MK_ERR_UNSUPPORTED, MK_ERR_NO_MEMORY, MK_ERR_CUDA
+ * (nothing is leaked on failure). */
 int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out);
 
-/* Forget the cached context: the cursor returns to slot 0 and the last id to 0.
- * Enqueued on `stream`; returns after the stream completes. */
+/* Forget the cached context: the cursor returns to slot 0 and the last id to 0
+ * (a new sequence; the KV cache of page A, "The idea: one kernel that never
+ * exits", starts empty).  Enqueued on `stream`; returns after the stream
+ * completes.  Errors: MK_ERR_INVALID_ARG (NULL, or a started decode not yet
+ * waited for), MK_ERR_CUDA. */
 int mk_reset_kv(mk_handle *h, mk_stream stream);
 
 /* Run n_in + n_steps forwards from the handle's cursor in ONE cooperative launch.
@@ -204,8 +219,9 @@ int mk_decode(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_ste
 
 /* Batched prompt prefill: the n forwards of mk_decode(h, d_in_ids, n, 0, ...)
  * computed all at once per layer instead of one token per forward -- the
- * projections as bf16 tensor-core GEMMs with fp32 accumulation (each fp32
- * activation enters as three bf16 terms, hi + mid + lo: all 24 bits), then
+ * projections as the library's own tcgen05 tensor-core GEMMs with fp32
+ * accumulation in tensor memory (each fp32 activation enters as three bf16
+ * terms, hi + mid + lo: all 24 bits, each in its own accumulator), then
  * QK-norm, RoPE / MRoPE,
  * the bf16 KV append and causal attention over the cache in the library's own
  * kernels.  It fills the same KV cache and advances the same cursor, so a
@@ -218,11 +234,13 @@ int mk_decode(mk_handle *h, const int32_t *d_in_ids, int32_t n_in, int32_t n_ste
  *   logits ([n][vocab]) and hidden ([n][L+1][H]) as for mk_decode; flags,
  *   trace and code rows must be unset.  Not bitwise equal to mk_decode (other
  *   summation orders); both follow the oracle within the parity tolerance.
- * The first call of a handle creates its GEMM library handle and scratch for
- * 256-token chunks (about 0.5 GB at the 0.6B shape); the launch sequence of
- * each prompt length is captured as a CUDA graph on its first use and replayed
+ * The first call of a handle creates its scratch for 256-token chunks (tens
+ * of MB at the 0.6B shape, plus V x 256 fp32 logits when every id is wanted)
+ * and the TMA descriptors of every weight matrix; the launch sequence of each
+ * prompt length is captured as a CUDA graph on its first use and replayed
  * afterwards (the call's ids, cursor and output pointers are read from device
- * memory, so a replay serves any call of that length).
+ * memory, so a replay serves any call of that length; at most 8 lengths are
+ * kept per handle, the least recently used replaced).
  * Blocks until `stream` completes.  Errors: MK_ERR_INVALID_ARG, MK_ERR_KV_FULL,
  * MK_ERR_BAD_TOKEN, MK_ERR_BAD_POSITION, MK_ERR_NUMERIC, MK_ERR_NO_MEMORY,
  * MK_ERR_UNSUPPORTED, MK_ERR_CUDA. */
@@ -253,17 +271,22 @@ int mk_decode_wait(mk_handle *h);
 int mk_mailbox_read(mk_handle *h, int32_t *dst, int32_t cap, int32_t *n_out);
 
 /* mk_decode with HOST id buffers: copies h_in_ids to the device, decodes and
- * copies the ids back to h_out_ids (n_in + n_steps entries).  The copies use
- * handle-owned staging; at most max_seq ids per call. */
+ * copies the ids back to h_out_ids (n_in + n_steps entries) -- the token-id
+ * input of page B, "Why Does a Single Kernel Even Matter for TTS?", from host
+ * memory.  The copies use handle-owned staging; at most max_seq ids per call.
+ * Errors: as mk_decode. */
 int mk_decode_host(mk_handle *h, const int32_t *h_in_ids, int32_t n_in, int32_t n_steps,
                    int32_t *h_out_ids, const mk_decode_opts *opts, mk_stream stream);
 
-/* Launch geometry, cursor and byte counts of a handle. */
+/* Launch geometry, cursor and byte counts of a handle (the bytes one forward
+ * streams: the quantity page B, "Why Does a Single Kernel Even Matter for
+ * TTS?", measures the kernel's bandwidth use by).  MK_ERR_INVALID_ARG on NULL. */
 int mk_get_info(const mk_handle *h, mk_info *info);
 
 /* Talker input rows: out[r] = sum_{j<n_books} books[j][codes[r][j]] + text[text_ids[r]],
  * accumulated in fp32 in table order (page B, "Why Does a Single Kernel Even
- * Matter for TTS?": inputs "are sums of 17 embeddings (16 codebooks + text)").
+ * Matter for TTS?": each talker input is the sum of the 16 codebook embeddings
+ * and the text embedding).
  * books: device bf16 [n_books][book_rows][H]; text: device bf16 [text_rows][H];
  * codes: device int32 [n][n_books]; text_ids: device int32 [n]; out: device fp32
  * [n][H].  Ids out of range give MK_ERR_BAD_TOKEN.  Blocks until `stream` completes. */
@@ -289,10 +312,13 @@ int mk_embed_sum_noalloc(const void *books, int32_t n_books, int32_t book_rows, 
                          int32_t text_rows, int32_t hidden, const int32_t *codes,
                          const int32_t *text_ids, int32_t n, float *out, mk_stream stream);
 
-/* Free everything the handle owns (not the borrowed weights).  NULL is a no-op. */
+/* Free everything the handle owns (not the borrowed weights): the end of the
+ * handle lifecycle that mk_create starts.  NULL is a no-op; always MK_OK. */
 int mk_destroy(mk_handle *h);
 
-/* Static string naming a status code. */
+/* Static string naming a status code (the error words the kernel sets instead
+ * of trapping, so that a failed step never takes the GPU down; the pages
+ * define no error model).  Unknown codes give "unknown error". */
 const char *mk_error_string(int code);
 
 #ifdef __cplusplus

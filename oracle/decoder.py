@@ -69,7 +69,7 @@ def pair_streams(head_dim: int, mrope_sections: Optional[Sequence[int]],
     """Which position stream drives each rotary pair ``i < d/2``.
 
     Plain RoPE: stream 0 for every pair.  MRoPE (page A, "Porting it to
-    Qwen3-TTS-1.7B": the talker "splits position encoding into sections"):
+    Qwen3-TTS-1.7B": the talker's rotary positions come in sections):
     contiguous runs of pair indices, ``sections[0]`` pairs on stream 0, the next
     ``sections[1]`` on stream 1, the rest on stream 2.
 
@@ -98,9 +98,9 @@ def rope_angles(positions, head_dim: int, theta: float,
     """Rotation angle of every pair: ``phi_i = pos_{s(i)} * theta^(-2i/d)``.
 
     ``positions`` is one position (plain RoPE) or three position-stream values.
-    The frequencies are the host-built table the talker needs ("RoPE freq?
-    Python tables only", page B, "So, What's the Catch with These
-    Megakernels?"), here in double precision."""
+    The frequencies are the host-built table the talker needs (page B, "So,
+    What's the Catch with These Megakernels?": rotary frequencies come from
+    tables built on the host), here in double precision."""
     half = head_dim // 2
     i = np.arange(half, dtype=F64)
     omega = np.power(F64(theta), -2.0 * i / head_dim)
@@ -155,8 +155,8 @@ def argmax_lowest(logits) -> int:
 
 def embed_sum17(codebooks_bits, text_bits, codes, text_ids) -> np.ndarray:
     """The talker's per-step input: the sum of 16 codebook embeddings and one
-    text embedding ("sums of 17 embeddings (16 codebooks + text)", page B,
-    "Why Does a Single Kernel Even Matter for TTS?").  Summed in table order
+    text embedding (page B, "Why Does a Single Kernel Even Matter for TTS?":
+    each talker input is that 17-way sum).  Summed in table order
     0..15 then text.  ``codes`` ``[n][16]``, ``text_ids`` ``[n]`` -> ``[n][H]``."""
     codes = np.asarray(codes)
     text_ids = np.asarray(text_ids)
@@ -178,8 +178,8 @@ def embed_sum17(codebooks_bits, text_bits, codes, text_ids) -> np.ndarray:
 @dataclass(frozen=True)
 class DecoderShape:
     """Dimensions of a Qwen3-style decoder (page B, "Why Does a Single Kernel
-    Even Matter for TTS?": the talker "mirrors Qwen3-0.6B exactly -- same dims,
-    layers, heads"; only vocab, RoPE frequencies and the untied head differ)."""
+    Even Matter for TTS?": the talker has Qwen3-0.6B's dimensions, layer count
+    and heads; only vocab, RoPE frequencies and the untied head differ)."""
     n_layers: int
     hidden: int
     n_q_heads: int
@@ -225,8 +225,9 @@ class Weights:
 def _input_row(W: Weights, token: int, sentinel_rows) -> np.ndarray:
     """Input embedding of one forward.  A non-negative id reads the embedding
     table; a negative id ``-(r+1)`` reads row ``r`` of the caller's precomputed
-    buffer ("If token_id >=0, lookup embedding. Else, grab precomputed from
-    buffer", page B, "Why Does a Single Kernel Even Matter for TTS?")."""
+    buffer (page B, "Why Does a Single Kernel Even Matter for TTS?": a
+    non-negative token id is looked up, anything else is taken precomputed from
+    a buffer)."""
     if token >= 0:
         return W.embed[token].copy()
     if sentinel_rows is None:

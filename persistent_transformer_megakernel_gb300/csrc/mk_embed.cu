@@ -1,8 +1,8 @@
 // Talker input rows for the negative-id sentinel: the sum of the codebook
-// embeddings and the text embedding of each step ("sums of 17 embeddings (16
-// codebooks + text)", page B = "I made a single CUDA kernel speak: streaming
-// Qwen3-TTS at 50ms latency on an RTX 5090", section "Why Does a Single
-// Kernel Even Matter for TTS?").  One CTA per row, fp32 accumulation in table
+// embeddings and the text embedding of each step (page B = "I made a single
+// CUDA kernel speak: streaming Qwen3-TTS at 50ms latency on an RTX 5090",
+// section "Why Does a Single Kernel Even Matter for TTS?": each talker input is
+// that 17-way sum).  One CTA per row, fp32 accumulation in table
 // order (codebook 0 .. n_books-1, then text).
 #include <cuda_runtime.h>
 

@@ -18,3 +18,12 @@ def cuda_device():
     if not torch.cuda.is_available():
         pytest.fail("GPU test run without a CUDA device")
     return torch.device("cuda:0")
+
+# The randomised oracle invariants need hypothesis, which only the CPU test
+# environment provides; where it is missing the module is not collected at all
+# (it holds CPU-only tests, so a GPU run loses nothing and reports no skip).
+collect_ignore = []
+try:
+    import hypothesis  # noqa: F401
+except ImportError:
+    collect_ignore.append("test_oracle_properties.py")
