@@ -553,7 +553,7 @@ def prefill_case(args):
     import persistent_transformer_megakernel_gb300 as mk
     wl, s, _ = workload_desc(args.workload)
     w = W.make_weights(s, seed=0)
-    n = wl["prompt"]
+    n = args.prefill_tokens if args.prefill_tokens > 0 else wl["prompt"]
     dec = mk.Decoder(s, w, max_seq=n + 8)
     prompt = torch.as_tensor(W.make_prompt(s["vocab_in"], n, seed=1), device="cuda")
     for rep in range(2):
@@ -599,6 +599,8 @@ def main():
     ap.add_argument("--ablation-forwards", type=int, default=32)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-ablation", action="store_true")
+    ap.add_argument("--prefill-tokens", type=int, default=0,
+                    help="prompt length of --prefill-case (default: the workload's prompt)")
     ap.add_argument("--prefill-case", action="store_true",
                     help="run the workload's prompt through mk_prefill twice (the prefill ncu launch list)")
     ap.add_argument("--trace-case", action="store_true",

@@ -130,3 +130,25 @@ def test_prefill_last_id_only_and_errors():
     with pytest.raises(mk.MKError):
         d.prefill(prompt)
     del full
+
+
+def test_prefill_graph_cache_stays_bounded_and_correct():
+    # more prompt lengths than the per-handle graph cache keeps (8): the least
+    # recently used graphs are replaced, and a length whose graph was dropped
+    # is captured again and still matches the oracle
+    s = W.shape("tiny")
+    w = W.make_weights(s, seed=0)
+    dec = mk.Decoder(s, w, max_seq=64)
+    lengths = list(range(3, 14))                    # 11 lengths
+    for n in lengths:
+        dec.reset()
+        dec.prefill(W.make_prompt(s["vocab_in"], n, seed=n),
+                    logits=torch.empty((n, s["vocab"]), device="cuda:0"))
+    p = W.make_prompt(s["vocab_in"], 3, seed=3)     # the first length: its graph was replaced
+    dec.reset()
+    lg = torch.full((3, s["vocab"]), float("nan"), device="cuda:0")
+    dec.prefill(p, logits=lg)
+    torch.cuda.synchronize()
+    pl, _, _, _ = O.prefix_forward(s, w, p)
+    assert_close(lg.double().cpu().numpy(), pl, "prefill after the graph cache turned over")
+    dec.close()
