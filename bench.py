@@ -38,8 +38,8 @@ PROFILES = os.path.join(ROOT, "profiles")
 
 # the files the decode kernel and its launch are built from; the prefill and
 # embedding kernels do not change what the decode kernel reads or writes
-DECODE_SOURCES = ("mk_device.cuh", "mk_host.cu", "mk_kernels_d128.cu", "mk_kernels_d64.cu", "mk_launch.h",
-                  "mk_params.h", "ptx.cuh")
+DECODE_SOURCES = ("mk_device.cuh", "mk_host.cu", "mk_kernels_d128.cu", "mk_kernels_d64.cu", "mk_kernels_hidden1024.cu",
+                  "mk_kernels_hidden2048.cu", "mk_launch.h", "mk_params.h", "mk_plans.h", "ptx.cuh")
 
 
 def kernel_sources_sha256():

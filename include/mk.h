@@ -185,6 +185,9 @@ typedef struct {
   int32_t max_chunks;    /* split-KV chunk capacity per kv head */
   int64_t weight_bytes;  /* bf16 bytes streamed per forward (layers + head) */
   int64_t kv_bytes;      /* KV-cache allocation */
+  int32_t plan;          /* decode kernel: 0 the general one (layouts chosen at run time,
+                            phases out of line), 1 compiled for hidden 1024 / MLP 3072 /
+                            16:8 heads of 128, 2 for hidden 2048 / MLP 6144 / 16:8 heads of 128 */
 } mk_info;
 
 /* Validate cfg, allocate the KV cache [L][Hkv][max_seq][d] bf16 (keys and

@@ -64,7 +64,8 @@ class mk_decode_opts(C.Structure):
 class mk_info(C.Structure):
     _fields_ = [("grid", C.c_int32), ("threads", C.c_int32), ("stages", C.c_int32),
                 ("stage_bytes", C.c_int32), ("smem_bytes", C.c_int32), ("position", C.c_int32),
-                ("max_chunks", C.c_int32), ("weight_bytes", C.c_int64), ("kv_bytes", C.c_int64)]
+                ("max_chunks", C.c_int32), ("weight_bytes", C.c_int64), ("kv_bytes", C.c_int64),
+                ("plan", C.c_int32)]
 
 
 #: every symbol include/mk.h declares

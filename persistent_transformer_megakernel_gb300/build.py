@@ -14,8 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmk.so")
-SOURCES = ["mk_host.cu", "mk_embed.cu", "mk_prefill.cu", "mk_gemm.cu", "mk_pfattn.cu", "mk_kernels_d64.cu",
-           "mk_kernels_d128.cu"]
+SOURCES = ["mk_kernels_d128.cu", "mk_kernels_hidden1024.cu", "mk_kernels_hidden2048.cu", "mk_kernels_d64.cu",
+           "mk_host.cu", "mk_embed.cu", "mk_prefill.cu", "mk_gemm.cu", "mk_pfattn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

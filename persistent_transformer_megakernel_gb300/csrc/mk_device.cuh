@@ -29,6 +29,7 @@
 #include <cmath>
 
 #include "mk_params.h"
+#include "mk_plans.h"
 #include "ptx.cuh"
 
 namespace mk {
@@ -722,10 +723,12 @@ __device__ __forceinline__ void ll_poll_pairs(const Params &p, SmemCtl &S, const
 // (layout 2): TPR = 256, one row group; each thread polls its own chunks.
 // Either way a thread keeps the partial dots of RPT rows of BT tiles in
 // registers and the warp reduces them once per batch; the partials of the
-// warps sharing a row (layout 2) meet in S.red before the epilogue.
+// warps sharing a row (layout 2) meet in S.red before the epilogue.  Inlined
+// into the plan kernels (kind a constant there); the general kernel calls the
+// out-of-line copy below.
 template <int KPT, int RPT, int BT, bool STAGED>
-__device__ __noinline__ void gemv_fast(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer, int f,
-                                       int cta, int in_id, unsigned tag, RingPos &rp, int &rb, int gp) {
+__device__ __forceinline__ void gemv_fast_body(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer,
+                                               int f, int cta, int in_id, unsigned tag, RingPos &rp, int &rb, int gp) {
   constexpr int CH = (KPT % 8 == 0) ? 8 : 4;
   constexpr int TPR = STAGED ? 32 : NCT;
   constexpr int NG = NCT / TPR;
@@ -904,6 +907,12 @@ __device__ __noinline__ void gemv_fast(const Params &p, SmemCtl &S, unsigned cha
     }
   }
   trace_mark(p, gp, cta, 2);
+}
+
+template <int KPT, int RPT, int BT, bool STAGED>
+__device__ __noinline__ void gemv_fast(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer, int f,
+                                       int cta, int in_id, unsigned tag, RingPos &rp, int &rb, int gp) {
+  gemv_fast_body<KPT, RPT, BT, STAGED>(p, S, ring, kind, layer, f, cta, in_id, tag, rp, rb, gp);
 }
 
 // dispatch on (KPT, RPTP) fixed at mk_create
@@ -1464,8 +1473,21 @@ struct Producer {
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int HD>
+// one GEMV phase: the plan's layout inline, or the general run-time dispatch
+template <class PL, int KIND>
+__device__ __forceinline__ void gemv_run(const Params &p, SmemCtl &S, unsigned char *ring, int layer, int f, int cta,
+                                         int in_id, unsigned tag, RingPos &rp, int &rb, int gp) {
+  if constexpr (PL::fixed) {
+    gemv_fast_body<PL::spec[KIND][1], PL::spec[KIND][2], PL::spec[KIND][3], PL::spec[KIND][0] == 1>(
+        p, S, ring, KIND, layer, f, cta, in_id, tag, rp, rb, gp);
+  } else {
+    gemv_dispatch(p, S, ring, KIND, layer, f, cta, in_id, tag, rp, rb, gp);
+  }
+}
+
+template <int HD, class PL>
 __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_constant__ Params pg) {
+  static_assert(!PL::fixed || PL::hd == HD, "a plan is compiled for its head_dim");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   SmemCtl &S = *reinterpret_cast<SmemCtl *>(smem_raw);
   unsigned char *ring = smem_raw + RING_OFFSET;
@@ -1599,7 +1621,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
     const unsigned tag = p.tag0 + static_cast<unsigned>(f);
     trace_mark(p, gp, cta, 0);
     if (ph == 5 * p.L) {
-      gemv_dispatch(p, S, ring, GV_LM, 0, f, cta, in_id, tag, rp, rb, gp);
+      gemv_run<PL, GV_LM>(p, S, ring, 0, f, cta, in_id, tag, rp, rb, gp);
       if (!p.per_op) {
         ok = grid_barrier(p, S, bar_target, f, cta);
         if (tid == 0) st_release_cta(&S.flags[F_FWD_DONE], f + 1);
@@ -1629,11 +1651,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
         as_f = f;
       }
       switch (k) {
-        case 0: gemv_dispatch(p, S, ring, GV_QKV, l, f, cta, in_id, tag, rp, rb, gp); break;
-        case 1: attention_dispatch<HD>(p, S, ring, l, f, cta, tag, rp, gp, as); break;
-        case 2: gemv_dispatch(p, S, ring, GV_O, l, f, cta, in_id, tag, rp, rb, gp); break;
-        case 3: gemv_dispatch(p, S, ring, GV_GU, l, f, cta, in_id, tag, rp, rb, gp); break;
-        default: gemv_dispatch(p, S, ring, GV_DOWN, l, f, cta, in_id, tag, rp, rb, gp); break;
+        case 0: gemv_run<PL, GV_QKV>(p, S, ring, l, f, cta, in_id, tag, rp, rb, gp); break;
+        case 1:
+          if constexpr (PL::fixed) attention_phase<HD, PL::grp>(p, S, ring, l, f, cta, tag, rp, gp, as);
+          else attention_dispatch<HD>(p, S, ring, l, f, cta, tag, rp, gp, as);
+          break;
+        case 2: gemv_run<PL, GV_O>(p, S, ring, l, f, cta, in_id, tag, rp, rb, gp); break;
+        case 3: gemv_run<PL, GV_GU>(p, S, ring, l, f, cta, in_id, tag, rp, rb, gp); break;
+        default: gemv_run<PL, GV_DOWN>(p, S, ring, l, f, cta, in_id, tag, rp, rb, gp); break;
       }
     }
     trace_mark(p, gp, cta, 3);

@@ -23,6 +23,7 @@
 #include "mk_launch.h"
 #include "mk_prefill.h"
 #include "mk_params.h"
+#include "mk_plans.h"
 
 namespace {
 
@@ -113,6 +114,24 @@ int make_geom(int K, int rows, bool pairs, mk::GemvGeom &g) {
 
 // The fast GEMV layouts compiled into the kernel (mk_device.cuh, gemv_dispatch):
 // {layout, KPT, rows per thread per tile, tiles per register batch}
+// The kernel for these layouts: a plan kernel whose compiled layouts and
+// attention group size are exactly these, else the general kernel.
+template <class PL>
+bool plan_matches(int d, int grp, const mk::GemvGeom *geo) {
+  if (PL::hd != d || PL::grp != grp) return false;
+  for (int k = 0; k < mk::GV_COUNT; ++k) {
+    const mk::GemvGeom &g = geo[k];
+    if (g.fast != PL::spec[k][0] || g.KPT != PL::spec[k][1] || g.RPTP != PL::spec[k][2] || g.BT != PL::spec[k][3])
+      return false;
+  }
+  return true;
+}
+const void *pick_kernel(int d, int grp, const mk::GemvGeom *geo) {
+  if (plan_matches<mk::PlanHidden1024>(d, grp, geo)) return mk::kernel_hidden1024();
+  if (plan_matches<mk::PlanHidden2048>(d, grp, geo)) return mk::kernel_hidden2048();
+  return d == 64 ? mk::kernel_d64() : mk::kernel_d128();
+}
+
 struct FastCase { int fast, kpt, rpt, bt; };
 const FastCase kFastCases[] = {{1, 32, 2, 4}, {1, 64, 1, 8}, {1, 16, 4, 2}, {1, 24, 2, 4}, {1, 8, 8, 1},
                                {2, 8, 8, 1},  {2, 8, 8, 2},  {2, 12, 4, 2}, {2, 24, 2, 8}};
@@ -334,7 +353,6 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
   cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device);
   if (!coop) return fail(MK_ERR_UNSUPPORTED);
   h->G = prop.multiProcessorCount;
-  h->kernel = (d == 64) ? mk::kernel_d64() : mk::kernel_d128();
   {
     // fast layouts where one fits (the general ones above stay otherwise)
     const int Ks[mk::GV_COUNT] = {H, Hq * d, H, I, H};
@@ -354,6 +372,7 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
       if (geo[k].fast == 2 && (geo[k].lgCH < 0 || geo[k].lgSpan < 0)) return fail(MK_ERR_UNSUPPORTED);
     }
   }
+  h->kernel = pick_kernel(d, Hq / Hkv, geo);
   // residual rows owned per CTA, and rows of every phase, must fit the static buffers
   if ((H + h->G - 1) / h->G > mk::MAX_OWN) return fail(MK_ERR_UNSUPPORTED);
   for (int k = 0; k < mk::GV_COUNT; ++k) {
@@ -756,6 +775,7 @@ int mk_get_info(const mk_handle *h, mk_info *info) {
   info->max_chunks = h->max_chunks;
   info->weight_bytes = h->weight_bytes;
   info->kv_bytes = h->kv_bytes;
+  info->plan = h->kernel == mk::kernel_hidden1024() ? 1 : h->kernel == mk::kernel_hidden2048() ? 2 : 0;
   return MK_OK;
 }
 

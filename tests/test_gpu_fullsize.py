@@ -50,6 +50,7 @@ def test_qwen3_0p6b_prompt32_greedy512():
     del ref
     feed = np.concatenate([prompt, ids_ref[31:543]]).astype(np.int32)
     dec = mk.Decoder(s, w, max_seq=544)
+    assert dec.info()["plan"] == 1   # the kernel compiled for these dims
     ids, lg, hd = _gpu_teacher_forced(dec, feed)
     _compare("qwen3_0p6b", s, ids, lg, hd, ids_ref, lg_ref, hd_ref)
     # free-running greedy in one launch: identical up to the oracle's first near tie
@@ -87,6 +88,7 @@ def test_tts_talker_sentinel_mrope_256():
     ref = O.Decoder(s, w, max_seq=n)
     ids_ref, lg_ref, hd_ref = ref.generate(sid, 0, sentinel_rows=E_ref, pos3=pos3)
     dec = mk.Decoder(s, w, max_seq=n)
+    assert dec.info()["plan"] == 1
     p3 = torch.as_tensor(pos3, device="cuda:0")
     ids, lg, hd = _gpu_teacher_forced(dec, sid, embeds=E, pos3=p3)
     _compare("tts_talker", s, ids, lg, hd, ids_ref, lg_ref, hd_ref)
@@ -112,6 +114,7 @@ def test_qwen3_1p7b_prompt32_greedy96():
     del ref
     feed = np.concatenate([prompt, ids_ref[31:127]]).astype(np.int32)
     dec = mk.Decoder(s, w, max_seq=128)
+    assert dec.info()["plan"] == 2   # the kernel compiled for these dims
     ids, lg, hd = _gpu_teacher_forced(dec, feed)
     _compare("qwen3_1p7b", s, ids, lg, hd, ids_ref, lg_ref, hd_ref)
     dec.close()

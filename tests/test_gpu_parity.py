@@ -32,6 +32,11 @@ def _run_gpu(dec, feed, n_steps=0, embeds=None, pos3=None, per_op=False, attn_ch
     return ids.cpu().numpy(), logits.double().cpu().numpy(), hidden.double().cpu().numpy()
 
 
+# the decode kernel mk_create picks: 1 = compiled for hidden 1024 / MLP 3072 /
+# 16:8 heads of 128 (every phase inline), 0 = the general kernel
+PLAN = {"mid": 1, "qwen3_0p6b": 1, "tts_talker": 1, "qwen3_1p7b": 2}
+
+
 def _teacher_forced(name, n_prompt, n_steps, max_seq=64, pos3_mode=None, per_op=False,
                     attn_chunks=0):
     s = W.shape(name)
@@ -43,6 +48,7 @@ def _teacher_forced(name, n_prompt, n_steps, max_seq=64, pos3_mode=None, per_op=
     ids_ref, lg_ref, hd_ref = ref.generate(prompt, n_steps, pos3=pos3)
     feed = np.concatenate([prompt, ids_ref[n_prompt - 1:n - 1]]).astype(np.int32)
     dec = mk.Decoder(s, w, max_seq=max_seq)
+    assert dec.info()["plan"] == PLAN.get(name, 0)
     p3 = None if pos3 is None else torch.as_tensor(pos3, device="cuda:0")
     ids, lg, hd = _run_gpu(dec, feed, 0, pos3=p3, per_op=per_op, attn_chunks=attn_chunks)
     assert_close(lg, lg_ref, name + " logits")
