@@ -80,6 +80,14 @@ struct RingPos {
   }
 };
 
+// the consumer's ring position and S.red buffer index, passed to and returned
+// from the out-of-line GEMV phases by value (in registers, not through the
+// caller's stack)
+struct RingState {
+  RingPos rp;
+  int rb = 0;
+};
+
 // balanced contiguous split of `total` items over G CTAs
 __device__ __forceinline__ void split_range(int total, int G, int cta, int &r0, int &r1) {
   r0 = static_cast<int>((static_cast<long long>(total) * cta) / G);
@@ -419,7 +427,9 @@ __device__ __forceinline__ void load_input_slice(const Params &p, int id, int k0
   }
 }
 
-__device__ __forceinline__ float input_elem(const Params &p, int id, int k) {
+// out of line: runs at layer 0 only, and its talker loop would otherwise sit
+// in every copy of the QKV code
+static __device__ __noinline__ float input_elem(const Params &p, int id, int k) {
   if (id >= 0) return bf2f(p.embed[static_cast<size_t>(id) * p.H + k]);
   if (!p.cb_codes) return p.embeds[static_cast<size_t>(-id - 1) * p.H + k];
   const int r = -id - 1;
@@ -501,8 +511,10 @@ __device__ __forceinline__ void gemv_epilogue(const Params &p, SmemCtl &S, const
 // Tiles are consumed without a CTA-wide barrier; row partials collect in a
 // batch buffer and one barrier per batch precedes the epilogue.
 template <int KPT, int RPTP>
-__device__ __noinline__ void gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer, int f,
-                           int cta, int in_id, unsigned tag, RingPos &rp, int &rb, int gp) {
+__device__ __noinline__ RingState gemv_phase(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer,
+                                             int f, int cta, int in_id, unsigned tag, RingState st, int gp) {
+  RingPos &rp = st.rp;
+  int &rb = st.rb;
   const GemvGeom g = p.geo[kind];
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int kc = t % g.TPR, rg = t / g.TPR;
@@ -620,6 +632,7 @@ __device__ __noinline__ void gemv_phase(const Params &p, SmemCtl &S, unsigned ch
     }
   }
   trace_mark(p, gp, cta, 2);
+  return st;
 }
 
 // ---------------------------------------------------------------------------
@@ -747,13 +760,16 @@ __device__ __forceinline__ void gemv_fast_body(const Params &p, SmemCtl &S, unsi
     const uint16_t *gain = kind == GV_QKV ? S.layers[layer].attn_norm
                          : kind == GV_GU  ? S.layers[layer].mlp_norm
                                           : p.final_norm;
-    float gn[KPT];
+    // kept as packed bf16 pairs across the poll (half the registers)
+    uint32_t gw[KPT / 2];
 #pragma unroll
     for (int c = 0; c < KPT / CH; ++c) {
-      float v[CH];
-      load_bf16<CH>(gain + c * SPAN + kc * CH, v);
 #pragma unroll
-      for (int j = 0; j < CH; ++j) gn[c * CH + j] = v[j];
+      for (int j = 0; j < CH / 4; ++j) {
+        const uint2 q = __ldg(reinterpret_cast<const uint2 *>(gain + c * SPAN + kc * CH) + j);
+        gw[(c * CH) / 2 + 2 * j] = q.x;
+        gw[(c * CH) / 2 + 2 * j + 1] = q.y;
+      }
     }
     // ---- the input vector into S.xs, with its sum of squares ---------------
     constexpr int MP = (KPT * 32 + 511) / 512;   // word pairs per thread
@@ -797,10 +813,11 @@ __device__ __forceinline__ void gemv_fast_body(const Params &p, SmemCtl &S, unsi
 #pragma unroll
       for (int j = 0; j < CH; j += 4) {
         const float4 q = *reinterpret_cast<const float4 *>(&S.xs[c * SPAN + kc * CH + j]);
-        xr[c * CH + j + 0] = q.x * rs * gn[c * CH + j + 0];
-        xr[c * CH + j + 1] = q.y * rs * gn[c * CH + j + 1];
-        xr[c * CH + j + 2] = q.z * rs * gn[c * CH + j + 2];
-        xr[c * CH + j + 3] = q.w * rs * gn[c * CH + j + 3];
+        const uint32_t g01 = gw[(c * CH + j) / 2], g23 = gw[(c * CH + j) / 2 + 1];
+        xr[c * CH + j + 0] = q.x * rs * bf_lo(g01);
+        xr[c * CH + j + 1] = q.y * rs * bf_hi(g01);
+        xr[c * CH + j + 2] = q.z * rs * bf_lo(g23);
+        xr[c * CH + j + 3] = q.w * rs * bf_hi(g23);
       }
     }
   } else {
@@ -909,31 +926,35 @@ __device__ __forceinline__ void gemv_fast_body(const Params &p, SmemCtl &S, unsi
   trace_mark(p, gp, cta, 2);
 }
 
+// the out-of-line copy: the general kernel's dispatch, and the plan kernels'
+// staged phases (QKV, gate/up and the LM head share one copy of the code)
 template <int KPT, int RPT, int BT, bool STAGED>
-__device__ __noinline__ void gemv_fast(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer, int f,
-                                       int cta, int in_id, unsigned tag, RingPos &rp, int &rb, int gp) {
-  gemv_fast_body<KPT, RPT, BT, STAGED>(p, S, ring, kind, layer, f, cta, in_id, tag, rp, rb, gp);
+__device__ __noinline__ RingState gemv_fast(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer,
+                                            int f, int cta, int in_id, unsigned tag, RingState st, int gp) {
+  gemv_fast_body<KPT, RPT, BT, STAGED>(p, S, ring, kind, layer, f, cta, in_id, tag, st.rp, st.rb, gp);
+  return st;
 }
 
 // dispatch on (KPT, RPTP) fixed at mk_create
-static __device__ __noinline__ void gemv_dispatch(const Params &p, SmemCtl &S, unsigned char *ring, int kind, int layer, int f,
-                              int cta, int in_id, unsigned tag, RingPos &rp, int &rb, int gp) {
+static __device__ __noinline__ RingState gemv_dispatch(const Params &p, SmemCtl &S, unsigned char *ring, int kind,
+                                                      int layer, int f, int cta, int in_id, unsigned tag, RingState st,
+                                                      int gp) {
   const int kpt = p.geo[kind].KPT, r = p.geo[kind].RPTP;
   if (p.geo[kind].fast) {
     // the fast layouts mk_create may pick (KPT, rows per thread per tile, tiles per batch)
     const int bt = p.geo[kind].BT;
 #define MK_FAST_CASE(ST, KP, RP, B) \
   if (p.geo[kind].fast == (ST ? 1 : 2) && kpt == KP && r == RP && bt == B) { \
-    gemv_fast<KP, RP, B, ST>(p, S, ring, kind, layer, f, cta, in_id, tag, rp, rb, gp); return; }
-    MK_FAST_CASE(true, 32, 2, 4) MK_FAST_CASE(true, 64, 1, 8) MK_FAST_CASE(true, 16, 4, 2)
+    return gemv_fast<KP, RP, B, ST>(p, S, ring, kind, layer, f, cta, in_id, tag, st, gp); }
+    MK_FAST_CASE(true, 32, 2, 2) MK_FAST_CASE(true, 64, 1, 8) MK_FAST_CASE(true, 16, 4, 2)
     MK_FAST_CASE(true, 24, 2, 4) MK_FAST_CASE(true, 8, 8, 1)
     MK_FAST_CASE(false, 8, 8, 1) MK_FAST_CASE(false, 8, 8, 2) MK_FAST_CASE(false, 12, 4, 2)
     MK_FAST_CASE(false, 24, 2, 8)
 #undef MK_FAST_CASE
-    return;
+    return st;
   }
 #define MK_GEMV_CASE(KP, RP) \
-  if (kpt == KP && r == RP) { gemv_phase<KP, RP>(p, S, ring, kind, layer, f, cta, in_id, tag, rp, rb, gp); return; }
+  if (kpt == KP && r == RP) return gemv_phase<KP, RP>(p, S, ring, kind, layer, f, cta, in_id, tag, st, gp);
   // every (KPT, RPTP) with KPT * RPTP <= 128 (mk_create rejects the others)
   MK_GEMV_CASE(8, 1) MK_GEMV_CASE(8, 2) MK_GEMV_CASE(8, 4) MK_GEMV_CASE(8, 8) MK_GEMV_CASE(8, 16)
   MK_GEMV_CASE(12, 1) MK_GEMV_CASE(12, 2) MK_GEMV_CASE(12, 4) MK_GEMV_CASE(12, 8)
@@ -942,6 +963,7 @@ static __device__ __noinline__ void gemv_dispatch(const Params &p, SmemCtl &S, u
   if constexpr (KPT_MAX >= 32) { MK_GEMV_CASE(32, 1) MK_GEMV_CASE(32, 2) MK_GEMV_CASE(32, 4) }
   if constexpr (KPT_MAX >= 48) { MK_GEMV_CASE(48, 1) MK_GEMV_CASE(48, 2) }
 #undef MK_GEMV_CASE
+  return st;
 }
 
 // ---------------------------------------------------------------------------
@@ -1473,15 +1495,20 @@ struct Producer {
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-// one GEMV phase: the plan's layout inline, or the general run-time dispatch
+// One GEMV phase.  Plan kernels: the split-K phases (O, down) inline, the
+// staged ones through one shared out-of-line copy (the instruction working
+// set of a forward is what limits the phase chain: three inline copies of the
+// staged code measured 9% slower).  General kernel: run-time dispatch.
 template <class PL, int KIND>
 __device__ __forceinline__ void gemv_run(const Params &p, SmemCtl &S, unsigned char *ring, int layer, int f, int cta,
-                                         int in_id, unsigned tag, RingPos &rp, int &rb, int gp) {
-  if constexpr (PL::fixed) {
-    gemv_fast_body<PL::spec[KIND][1], PL::spec[KIND][2], PL::spec[KIND][3], PL::spec[KIND][0] == 1>(
-        p, S, ring, KIND, layer, f, cta, in_id, tag, rp, rb, gp);
+                                         int in_id, unsigned tag, RingState &st, int gp) {
+  constexpr int fast = PL::spec[KIND][0], kpt = PL::spec[KIND][1], rpt = PL::spec[KIND][2], bt = PL::spec[KIND][3];
+  if constexpr (PL::fixed && fast == 1) {
+    st = gemv_fast<kpt, rpt, bt, true>(p, S, ring, KIND, layer, f, cta, in_id, tag, st, gp);
+  } else if constexpr (PL::fixed) {
+    gemv_fast_body<kpt, rpt, bt, false>(p, S, ring, KIND, layer, f, cta, in_id, tag, st.rp, st.rb, gp);
   } else {
-    gemv_dispatch(p, S, ring, KIND, layer, f, cta, in_id, tag, rp, rb, gp);
+    st = gemv_dispatch(p, S, ring, KIND, layer, f, cta, in_id, tag, st, gp);
   }
 }
 
@@ -1609,8 +1636,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
   // Phases hand their outputs to the next phase as tagged words (no barrier);
   // only the LM head ends with a grid barrier, which publishes the argmax
   // candidates and orders this forward's KV-cache writes before the next one.
-  RingPos rp;
-  int rb = 0;
+  RingState st;
+  RingPos &rp = st.rp;
   unsigned bar_target = 0;
   int in_id = 0;
   bool ok = true;
@@ -1621,7 +1648,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
     const unsigned tag = p.tag0 + static_cast<unsigned>(f);
     trace_mark(p, gp, cta, 0);
     if (ph == 5 * p.L) {
-      gemv_run<PL, GV_LM>(p, S, ring, 0, f, cta, in_id, tag, rp, rb, gp);
+      gemv_run<PL, GV_LM>(p, S, ring, 0, f, cta, in_id, tag, st, gp);
       if (!p.per_op) {
         ok = grid_barrier(p, S, bar_target, f, cta);
         if (tid == 0) st_release_cta(&S.flags[F_FWD_DONE], f + 1);
@@ -1651,14 +1678,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
         as_f = f;
       }
       switch (k) {
-        case 0: gemv_run<PL, GV_QKV>(p, S, ring, l, f, cta, in_id, tag, rp, rb, gp); break;
+        case 0: gemv_run<PL, GV_QKV>(p, S, ring, l, f, cta, in_id, tag, st, gp); break;
         case 1:
           if constexpr (PL::fixed) attention_phase<HD, PL::grp>(p, S, ring, l, f, cta, tag, rp, gp, as);
           else attention_dispatch<HD>(p, S, ring, l, f, cta, tag, rp, gp, as);
           break;
-        case 2: gemv_run<PL, GV_O>(p, S, ring, l, f, cta, in_id, tag, rp, rb, gp); break;
-        case 3: gemv_run<PL, GV_GU>(p, S, ring, l, f, cta, in_id, tag, rp, rb, gp); break;
-        default: gemv_run<PL, GV_DOWN>(p, S, ring, l, f, cta, in_id, tag, rp, rb, gp); break;
+        case 2: gemv_run<PL, GV_O>(p, S, ring, l, f, cta, in_id, tag, st, gp); break;
+        case 3: gemv_run<PL, GV_GU>(p, S, ring, l, f, cta, in_id, tag, st, gp); break;
+        default: gemv_run<PL, GV_DOWN>(p, S, ring, l, f, cta, in_id, tag, st, gp); break;
       }
     }
     trace_mark(p, gp, cta, 3);

@@ -133,7 +133,7 @@ const void *pick_kernel(int d, int grp, const mk::GemvGeom *geo) {
 }
 
 struct FastCase { int fast, kpt, rpt, bt; };
-const FastCase kFastCases[] = {{1, 32, 2, 4}, {1, 64, 1, 8}, {1, 16, 4, 2}, {1, 24, 2, 4}, {1, 8, 8, 1},
+const FastCase kFastCases[] = {{1, 32, 2, 2}, {1, 64, 1, 8}, {1, 16, 4, 2}, {1, 24, 2, 4}, {1, 8, 8, 1},
                                {2, 8, 8, 1},  {2, 8, 8, 2},  {2, 12, 4, 2}, {2, 24, 2, 8}};
 
 // A fast layout for one GEMV phase, if one fits: the RMSNorm-fused phases

@@ -18,7 +18,7 @@ struct PlanHidden1024 {
   // dims, which the TTS talker mirrors): any vocabulary
   static constexpr bool fixed = true;
   static constexpr int hd = 128, grp = 2;
-  static constexpr int spec[5][4] = {{1, 32, 2, 4}, {2, 8, 8, 1}, {1, 32, 2, 4}, {2, 12, 4, 2}, {1, 32, 2, 4}};
+  static constexpr int spec[5][4] = {{1, 32, 2, 2}, {2, 8, 8, 1}, {1, 32, 2, 2}, {2, 12, 4, 2}, {1, 32, 2, 2}};
 };
 
 struct PlanHidden2048 {
