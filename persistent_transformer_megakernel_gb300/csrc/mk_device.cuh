@@ -946,7 +946,7 @@ static __device__ __noinline__ RingState gemv_dispatch(const Params &p, SmemCtl 
 #define MK_FAST_CASE(ST, KP, RP, B) \
   if (p.geo[kind].fast == (ST ? 1 : 2) && kpt == KP && r == RP && bt == B) { \
     return gemv_fast<KP, RP, B, ST>(p, S, ring, kind, layer, f, cta, in_id, tag, st, gp); }
-    MK_FAST_CASE(true, 32, 2, 2) MK_FAST_CASE(true, 64, 1, 8) MK_FAST_CASE(true, 16, 4, 2)
+    MK_FAST_CASE(true, 32, 2, 2) MK_FAST_CASE(true, 64, 1, 4) MK_FAST_CASE(true, 16, 4, 2)
     MK_FAST_CASE(true, 24, 2, 4) MK_FAST_CASE(true, 8, 8, 1)
     MK_FAST_CASE(false, 8, 8, 1) MK_FAST_CASE(false, 8, 8, 2) MK_FAST_CASE(false, 12, 4, 2)
     MK_FAST_CASE(false, 24, 2, 8)
@@ -1506,7 +1506,7 @@ __device__ __forceinline__ void gemv_run(const Params &p, SmemCtl &S, unsigned c
   if constexpr (PL::fixed && fast == 1) {
     st = gemv_fast<kpt, rpt, bt, true>(p, S, ring, KIND, layer, f, cta, in_id, tag, st, gp);
   } else if constexpr (PL::fixed) {
-    gemv_fast_body<kpt, rpt, bt, false>(p, S, ring, KIND, layer, f, cta, in_id, tag, st.rp, st.rb, gp);
+    gemv_fast_body<kpt, rpt, bt, fast == 1>(p, S, ring, KIND, layer, f, cta, in_id, tag, st.rp, st.rb, gp);
   } else {
     st = gemv_dispatch(p, S, ring, KIND, layer, f, cta, in_id, tag, st, gp);
   }

@@ -132,8 +132,13 @@ const void *pick_kernel(int d, int grp, const mk::GemvGeom *geo) {
   return d == 64 ? mk::kernel_d64() : mk::kernel_d128();
 }
 
+// {fast (1 staged, 2 split-K), KPT, rows per thread per tile, tiles per
+// batch}.  Tiles per batch set how much of the tile loop is unrolled: the
+// staged layouts at width 1024 and 2048 were swept on the GB300 (0.6B: 1 and
+// 2 equal, 4 slower by 9%; 1.7B: 4 fastest, 1/2/8 slower by 9/4/10%); the
+// results do not depend on it.
 struct FastCase { int fast, kpt, rpt, bt; };
-const FastCase kFastCases[] = {{1, 32, 2, 2}, {1, 64, 1, 8}, {1, 16, 4, 2}, {1, 24, 2, 4}, {1, 8, 8, 1},
+const FastCase kFastCases[] = {{1, 32, 2, 2}, {1, 64, 1, 4}, {1, 16, 4, 2}, {1, 24, 2, 4}, {1, 8, 8, 1},
                                {2, 8, 8, 1},  {2, 8, 8, 2},  {2, 12, 4, 2}, {2, 24, 2, 8}};
 
 // A fast layout for one GEMV phase, if one fits: the RMSNorm-fused phases

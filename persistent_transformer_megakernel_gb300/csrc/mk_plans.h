@@ -25,7 +25,7 @@ struct PlanHidden2048 {
   // hidden 2048, 16 query / 8 KV heads of 128, MLP 6144 (the Qwen3-1.7B dims)
   static constexpr bool fixed = true;
   static constexpr int hd = 128, grp = 2;
-  static constexpr int spec[5][4] = {{1, 64, 1, 8}, {2, 8, 8, 2}, {1, 64, 1, 8}, {2, 24, 2, 8}, {1, 64, 1, 8}};
+  static constexpr int spec[5][4] = {{1, 64, 1, 4}, {2, 8, 8, 2}, {1, 64, 1, 4}, {2, 24, 2, 8}, {1, 64, 1, 4}};
 };
 
 struct PlanGeneral {
