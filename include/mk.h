@@ -148,8 +148,8 @@ typedef struct {
                                  phase: after the grid barrier that closes the forward);
                                  or NULL */
   int32_t attn_chunks;        /* split-KV chunks per kv head; 0 = the library's policy
-                                 (4 chunks up to 1024 cached positions, then one chunk
-                                 per 256 positions up to grid / n_kv_heads; up to 8
+                                 (at least 4, one per 48 cached positions up to 8, then
+                                 one per 256 positions up to grid / n_kv_heads; up to 8
                                  chunks merge by polling, more by the last CTA) */
   int64_t spin_ns;            /* budget of every device wait; 0 = 1 s */
   int32_t fault_skip_barrier; /* test hook: N > 0 makes CTA 0 skip its arrival at the

@@ -59,6 +59,11 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
   return static_cast<uint16_t>(u >> 16);
 }
 
+// 1 / sqrt(x), each step correctly rounded: the same value as 1.0f / sqrtf(x)
+// under IEEE division and square root, without the general division's
+// scaling path (about 300 cycles on the critical path of every norm)
+__device__ __forceinline__ float inv_sqrt_rn(float x) { return __frcp_rn(__fsqrt_rn(x)); }
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -556,7 +561,7 @@ __device__ __noinline__ RingState gemv_phase(const Params &p, SmemCtl &S, unsign
 #pragma unroll
     for (int i = 0; i < NCW; ++i) tot += S.misc[i];
     const float ms = g.invK != 0.f ? tot * g.invK : tot / static_cast<float>(g.K);   // identical for 2^n
-    const float rs = 1.0f / sqrtf(ms + p.eps);
+    const float rs = inv_sqrt_rn(ms + p.eps);
 #pragma unroll
     for (int j = 0; j < KPT; ++j) xr[j] = xr[j] * rs * gn[j];
   }
@@ -807,7 +812,7 @@ __device__ __forceinline__ void gemv_fast_body(const Params &p, SmemCtl &S, unsi
 #pragma unroll
     for (int i = 0; i < NCW; ++i) tot += S.misc[i];
     const float ms = g.invK != 0.f ? tot * g.invK : tot / static_cast<float>(g.K);   // identical for 2^n
-    const float rs = 1.0f / sqrtf(ms + p.eps);
+    const float rs = inv_sqrt_rn(ms + p.eps);
 #pragma unroll
     for (int c = 0; c < KPT / CH; ++c) {
 #pragma unroll
@@ -838,7 +843,7 @@ __device__ __forceinline__ void gemv_fast_body(const Params &p, SmemCtl &S, unsi
   }
   trace_mark(p, gp, cta, 1);
 
-  const int ntiles = (r1 - r0 + g.RT - 1) / g.RT;
+  const int ntiles = S.nt[kind];
   const int trow = (kind == GV_GU) ? 2 * g.RT : g.RT;       // rows of a full tile
   const size_t rowb = static_cast<size_t>(g.K) * 2;
   float best_v = -INFINITY;
@@ -971,6 +976,7 @@ static __device__ __noinline__ RingState gemv_dispatch(const Params &p, SmemCtl 
 // ---------------------------------------------------------------------------
 struct AttnSched {
   int P, ctx, cs, C, units;
+  int g0, c0;   // head and chunk of this CTA's first unit (unit = blockIdx.x)
 };
 
 __device__ __forceinline__ AttnSched attn_sched(const Params &p, int f) {
@@ -978,15 +984,20 @@ __device__ __forceinline__ AttnSched attn_sched(const Params &p, int f) {
   a.P = p.pos0 + f;
   a.ctx = a.P + 1;
   int cmax = p.chunks_override > 0 ? p.chunks_override : max(1, p.G / p.Hkv);
-  // up to attn_min_chunks * attn_ppc positions: attn_min_chunks chunks; longer
-  // contexts: one chunk per attn_ppc positions (up to poll_cm chunks merge by
-  // polling, more by the last-arriving CTA)
-  if (p.chunks_override <= 0 && p.attn_ppc > 0)
-    cmax = min(cmax, max((a.ctx + p.attn_ppc - 1) / p.attn_ppc, min(p.attn_min_chunks, a.ctx)));
+  // at least attn_min_chunks chunks, and one per attn_short_ppc positions up to
+  // poll_cm chunks; beyond poll_cm * attn_ppc positions one per attn_ppc (up
+  // to poll_cm chunks merge by polling, more by the last-arriving CTA)
+  if (p.chunks_override <= 0 && p.attn_ppc > 0) {
+    int want = max((a.ctx + p.attn_ppc - 1) / p.attn_ppc, min(p.attn_min_chunks, a.ctx));
+    if (p.attn_short_ppc > 0) want = max(want, min(p.poll_cm, (a.ctx + p.attn_short_ppc - 1) / p.attn_short_ppc));
+    cmax = min(cmax, want);
+  }
   cmax = min(cmax, p.max_chunks);
   a.cs = (a.ctx + cmax - 1) / cmax;
   a.C = (a.ctx + a.cs - 1) / a.cs;
   a.units = p.Hkv * a.C;
+  a.g0 = static_cast<int>(blockIdx.x) / a.C;
+  a.c0 = static_cast<int>(blockIdx.x) - a.g0 * a.C;
   return a;
 }
 
@@ -1016,12 +1027,13 @@ __device__ __forceinline__ int stream_pos(const Params &p, int f, int s, int P) 
 template <int HD>
 __device__ __forceinline__ void norm_rope_head(const Params &p, float (&v)[HD / 32], const float (&gain)[HD / 32],
                                                const float2 (&cs)[HD / 64]) {
+  static_assert((HD & (HD - 1)) == 0, "head_dim a power of two");
   constexpr int EPL = HD / 32;
   float ss = 0.f;
 #pragma unroll
   for (int k = 0; k < EPL; ++k) ss = fmaf(v[k], v[k], ss);
   ss = warp_sum(ss);
-  const float rs = 1.0f / sqrtf(ss / static_cast<float>(HD) + p.eps);
+  const float rs = inv_sqrt_rn(ss * (1.0f / static_cast<float>(HD)) + p.eps);   // HD a power of two: = ss / HD
 #pragma unroll
   for (int k = 0; k < EPL; ++k) v[k] = v[k] * rs * gain[k];
 #pragma unroll
@@ -1109,6 +1121,27 @@ static __device__ __noinline__ float merge_polled_chunks(const Params &p, SmemCt
   return os / lsum;
 }
 
+// The last CTA of kv head g merges its C chunk states from p.part (the same
+// arithmetic as merge_polled_chunks); out of line: only long contexts (more
+// chunks than the polled merge takes) run it.
+static __device__ __noinline__ void merge_ticket_chunks(const Params &p, unsigned long long *attn_ll, int g, int grp,
+                                                        int hd, int C, unsigned tag) {
+  for (int e = threadIdx.x; e < grp * hd; e += NCT) {
+    const int h = e / hd, i = e - h * hd;
+    const int j = g * grp + h;
+    const float *src = p.part + static_cast<size_t>(j) * p.max_chunks * (hd + 2);
+    float M = -INFINITY;
+    for (int cc = 0; cc < C; ++cc) M = fmaxf(M, __ldcg(src + cc * (hd + 2) + hd));
+    float os = 0.f, lsum = 0.f;
+    for (int cc = 0; cc < C; ++cc) {
+      const float sc = expf(__ldcg(src + cc * (hd + 2) + hd) - M);
+      os = fmaf(sc, __ldcg(src + cc * (hd + 2) + i), os);
+      lsum = fmaf(sc, __ldcg(src + cc * (hd + 2) + hd + 1), lsum);
+    }
+    ll_store_rep(p, attn_ll + ll_slot(p.geo[GV_O], j * hd + i), os / lsum, tag);
+  }
+}
+
 template <int HD, int GRP>
 __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring, int l, int f, int cta,
                                 unsigned tag, RingPos &rp, int gp, const AttnSched &as) {
@@ -1124,7 +1157,9 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
   unsigned long long *attn_ll = p.ll.attn + static_cast<size_t>(l) * p.Hq * HD;
 
   for (int u = cta; u < as.units; u += p.G) {
-    const int g = u / as.C, c = u % as.C;
+    // (a division costs hundreds of cycles here: the first unit's indices come with the schedule)
+    const int g = u == cta ? as.g0 : u / as.C;
+    const int c = u == cta ? as.c0 : u - g * as.C;
     const int a = c * as.cs, b = min(a + as.cs, as.ctx);
     const int pend = min(b, P);                // positions < P come through the ring
     const bool has_cur = (b == as.ctx);        // this chunk holds the new position P
@@ -1147,27 +1182,20 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
       float v[EPL];
 #pragma unroll
       for (int k = 0; k < EPL; ++k) v[k] = ll_val(wv[k]);
+      if (job <= GRP) norm_rope_head<HD>(p, v, gv, csv);
       if (job < GRP) {
-        norm_rope_head<HD>(p, v, gv, csv);
 #pragma unroll
         for (int k = 0; k < EPL; ++k) S.qs[job * HD + lane + 32 * k] = v[k] * p.inv_sqrt_d;
-      } else if (job == GRP) {
-        norm_rope_head<HD>(p, v, gv, csv);
-        uint16_t *dst = p.kcache + ((static_cast<size_t>(l) * p.Hkv + g) * p.max_seq + P) * HD;
-#pragma unroll
-        for (int k = 0; k < EPL; ++k) {
-          const uint16_t bb = f2bf(v[k]);
-          dst[lane + 32 * k] = bb;
-          S.kcur[lane + 32 * k] = bf2f(bb);
-        }
-        fence_proxy_async_global();
       } else {
-        uint16_t *dst = p.vcache + ((static_cast<size_t>(l) * p.Hkv + g) * p.max_seq + P) * HD;
+        // this position's key (job GRP) or value, rounded to bf16 into the cache
+        uint16_t *dst = (job == GRP ? p.kcache : p.vcache) +
+                        ((static_cast<size_t>(l) * p.Hkv + g) * p.max_seq + P) * HD;
+        float *cur = job == GRP ? S.kcur : S.vcur;
 #pragma unroll
         for (int k = 0; k < EPL; ++k) {
           const uint16_t bb = f2bf(v[k]);
           dst[lane + 32 * k] = bb;
-          S.vcur[lane + 32 * k] = bf2f(bb);
+          cur[lane + 32 * k] = bf2f(bb);
         }
         fence_proxy_async_global();
       }
@@ -1219,9 +1247,9 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
       const unsigned char *st = ring + static_cast<size_t>(slot) * STAGE_BYTES;
       const uint16_t *kt = reinterpret_cast<const uint16_t *>(st) + lane * EPL;
       const uint16_t *vt = kt + static_cast<size_t>(np) * HD;
-      int i = w;
       // two positions at a time: their scores' warp reductions overlap; the
       // updates still run in position order (the same arithmetic as one by one)
+      int i = w;
       for (; i + NCW < np; i += 2 * NCW) {
         float kk[2][EPL], vv[2][EPL], sv[2][GRP];
 #pragma unroll
@@ -1311,22 +1339,7 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
         flag(S, F_LAST) = last;
       }
       cons_sync();
-      if (flag(S, F_LAST)) {
-        for (int e = t; e < GRP * HD; e += NCT) {
-          const int h = e / HD, i = e % HD;
-          const int j = g * GRP + h;
-          const float *src = p.part + static_cast<size_t>(j) * p.max_chunks * (HD + 2);
-          float M = -INFINITY;
-          for (int cc = 0; cc < as.C; ++cc) M = fmaxf(M, __ldcg(src + cc * (HD + 2) + HD));
-          float os = 0.f, lsum = 0.f;
-          for (int cc = 0; cc < as.C; ++cc) {
-            const float sc = expf(__ldcg(src + cc * (HD + 2) + HD) - M);
-            os = fmaf(sc, __ldcg(src + cc * (HD + 2) + i), os);
-            lsum = fmaf(sc, __ldcg(src + cc * (HD + 2) + HD + 1), lsum);
-          }
-          ll_store_rep(p, attn_ll + ll_slot(p.geo[GV_O], j * HD + i), os / lsum, tag);
-        }
-      }
+      if (flag(S, F_LAST)) merge_ticket_chunks(p, attn_ll, g, GRP, HD, as.C, tag);
     }
   }
   trace_mark(p, gp, cta, 2);
@@ -1571,7 +1584,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
     fence_mbar_init();
     // this CTA's rows of every GEMV phase (the O and down ranges are also the
     // residual rows it owns), computed once instead of in every phase
-    for (int k = 0; k < GV_COUNT; ++k) split_range(p.geo[k].rows, p.G, cta, S.rr[k][0], S.rr[k][1]);
+    for (int k = 0; k < GV_COUNT; ++k) {
+      split_range(p.geo[k].rows, p.G, cta, S.rr[k][0], S.rr[k][1]);
+      S.nt[k] = (S.rr[k][1] - S.rr[k][0] + p.geo[k].RT - 1) / p.geo[k].RT;
+    }
     flag(S, F_ABORT) = (p.per_op && ld_relaxed_i32(p.err) != 0) ? 1 : 0;
     flag(S, F_PROD_DONE) = 0;
     flag(S, F_FWD_DONE) = p.per_op ? INT_MAX : 0;

@@ -32,9 +32,12 @@ constexpr int kMaxStagesWanted = 6;
 // split-KV: MAX_POLL_CHUNKS chunks up to MAX_POLL_CHUNKS * this many cached
 // positions, one chunk per this many beyond
 constexpr int kAttnPositionsPerChunk = 256;
-// split-KV chunks of a short context (measured on the 0.6B shape at 33..160
-// cached positions: 2/3/4/5/6/8 chunks gave 679/670/668/671/677/683 us/token)
+// split-KV chunks of a short context: at least 4, and one per 48 positions up
+// to the 8 that merge by polling (measured on the 0.6B shape, us/token with a
+// fixed chunk count 1/2/3/4/6/8: 564/538/530/522/522/523 at 33..288 cached
+// positions, -/579/552/540/533/532 at 33..544)
 constexpr int kShortContextChunks = 4;
+constexpr int kShortPositionsPerChunk = 48;
 constexpr int kMinChunks = 64;
    // split-KV chunk capacity per kv head (at least grid / Hkv)
 
@@ -501,6 +504,7 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
   p.attn_ppc = attn_ppc;
   p.poll_cm = mk::MAX_POLL_CHUNKS;
   p.attn_min_chunks = kShortContextChunks;
+  p.attn_short_ppc = kShortPositionsPerChunk;
   p.part = part;
   p.cand_val = cand_val; p.cand_idx = cand_idx; p.tickets = tickets;
   p.bar = reinterpret_cast<unsigned *>(h->d_sync);

@@ -145,6 +145,7 @@ struct Params {
   int poll_cm;                     // chunk counts in (1, poll_cm] merge by polling; more: ticket merge
   int attn_ppc;                    // target cached positions per split-KV chunk (0: one chunk per CTA share)
   int attn_min_chunks;             // chunks of a short context (fewer than attn_ppc positions each)
+  int attn_short_ppc;              // and at least ceil(ctx / this) chunks, up to poll_cm
   long long spin_ns;
   int fault_barrier;
   int G;                           // CTAs
@@ -168,6 +169,7 @@ struct SmemCtl {
   float misc[64];
   float xown[MAX_OWN];                   // residual rows this CTA owns
   int rr[GV_COUNT][2];                   // this CTA's row range of every GEMV phase
+  int nt[GV_COUNT];                      // and its tile count (RT rows a tile)
   int flags[F_COUNT];
   float bestv[NCW];
   int besti[NCW];
