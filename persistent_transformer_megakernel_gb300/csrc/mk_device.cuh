@@ -103,7 +103,8 @@ __device__ __forceinline__ void split_range(int total, int G, int cta, int &r0, 
 // halving steps lane l holds row (l >> (5 - log2 N)), summed over the warp.
 template <int N>
 __device__ __forceinline__ float warp_multi_reduce(float (&v)[N], int lane) {
-  constexpr int LOGN = (N >= 16) ? 4 : (N >= 8) ? 3 : (N >= 4) ? 2 : (N >= 2) ? 1 : 0;
+  constexpr int LOGN = (N >= 32) ? 5 : (N >= 16) ? 4 : (N >= 8) ? 3 : (N >= 4) ? 2 : (N >= 2) ? 1 : 0;
+  static_assert(N == (1 << LOGN) && N <= 32, "slots: a power of two up to 32");
 #pragma unroll
   for (int lvl = 0; lvl < LOGN; ++lvl) {
     const int o = 16 >> lvl;
@@ -1190,12 +1191,12 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
         // this position's key (job GRP) or value, rounded to bf16 into the cache
         uint16_t *dst = (job == GRP ? p.kcache : p.vcache) +
                         ((static_cast<size_t>(l) * p.Hkv + g) * p.max_seq + P) * HD;
-        float *cur = job == GRP ? S.kcur : S.vcur;
+        uint16_t *cur = job == GRP ? S.kcur : S.vcur;
 #pragma unroll
         for (int k = 0; k < EPL; ++k) {
           const uint16_t bb = f2bf(v[k]);
           dst[lane + 32 * k] = bb;
-          cur[lane + 32 * k] = bf2f(bb);
+          cur[lane + 32 * k] = bb;
         }
         fence_proxy_async_global();
       }
@@ -1203,7 +1204,14 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
     cons_sync();
     trace_mark(p, gp, cta, 1);
 
-    // ---- scores and online softmax, one warp per position --------------------
+    // ---- scores and online softmax, 8 positions per warp at a time -----------
+    // Lane l holds dims l*EPL .. l*EPL+EPL-1 of q, of every key and value row
+    // and of the output.  A block of 8 positions: per-lane partial scores of
+    // the 8 x GRP (head, position) pairs, one multi-slot warp reduction (lane
+    // holds slot (h * 8 + j) after it), the block's maximum and sum per head
+    // by shuffles among the lanes of a head, then the rescaled output update.
+    constexpr int NSL = 8 * GRP;
+    constexpr int LPS = NSL >= 32 ? 0 : NSL >= 16 ? 1 : NSL >= 8 ? 2 : 3;   // log2 lanes per slot
     float q[GRP][EPL], o[GRP][EPL], m[GRP], ls[GRP];
 #pragma unroll
     for (int h = 0; h < GRP; ++h) {
@@ -1212,77 +1220,72 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
       m[h] = -INFINITY;
       ls[h] = 0.f;
     }
-    // score of one cached position for every head of the group (warp-reduced)
-    auto score = [&](const float (&kk)[EPL], float (&sv)[GRP]) {
+    // positions j < nv of rows kb + j * HD (keys) and vb + j * HD (values)
+    auto block = [&](const uint16_t *kb, const uint16_t *vb, int nv) {
+      float sp[NSL], vv[8][EPL];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int jj = min(j, nv - 1);        // past the last position: re-read it, masked below
+        float kk[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          kk[e] = bf2f(kb[jj * HD + lane * EPL + e]);
+          vv[j][e] = bf2f(vb[jj * HD + lane * EPL + e]);
+        }
+#pragma unroll
+        for (int h = 0; h < GRP; ++h) {
+          float x = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) x = fmaf(q[h][e], kk[e], x);
+          sp[h * 8 + j] = x;
+        }
+      }
+      const float sv = warp_multi_reduce<NSL>(sp, lane);
+      const int sl = lane >> LPS, hj = sl >> 3, jl = sl & 7;
+      const bool valid = jl < nv;
+      // block maximum of each head, then the new running maximum
+      float bm = valid ? sv : -INFINITY;
+#pragma unroll
+      for (int off = 1 << LPS; off < (8 << LPS); off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
+      float mn[GRP], sc[GRP];
+      float m_own = 0.f;
 #pragma unroll
       for (int h = 0; h < GRP; ++h) {
-        float x = 0.f;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) x = fmaf(q[h][e], kk[e], x);
-        sv[h] = warp_sum(x);
+        mn[h] = fmaxf(m[h], __shfl_sync(0xffffffffu, bm, (h * 8) << LPS));
+        sc[h] = expf(m[h] - mn[h]);
+        if (hj == h) m_own = mn[h];
       }
-    };
-    // online-softmax update with one position's scores and value row
-    auto update = [&](const float (&sv)[GRP], const float (&vv)[EPL]) {
+      const float pe = valid ? expf(sv - m_own) : 0.f;
+      float bs = pe;
+#pragma unroll
+      for (int off = 1 << LPS; off < (8 << LPS); off <<= 1) bs += __shfl_xor_sync(0xffffffffu, bs, off);
 #pragma unroll
       for (int h = 0; h < GRP; ++h) {
-        const float mn = fmaxf(m[h], sv[h]);
-        const float sc = expf(m[h] - mn);
-        const float pe = expf(sv[h] - mn);
-        ls[h] = ls[h] * sc + pe;
+        ls[h] = ls[h] * sc[h] + __shfl_sync(0xffffffffu, bs, (h * 8) << LPS);
+        m[h] = mn[h];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) o[h][e] = fmaf(pe, vv[e], o[h][e] * sc);
-        m[h] = mn;
+        for (int e = 0; e < EPL; ++e) o[h][e] *= sc[h];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float pj = __shfl_sync(0xffffffffu, pe, (h * 8 + j) << LPS);
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) o[h][e] = fmaf(pj, vv[j][e], o[h][e]);
+        }
       }
-    };
-    auto visit = [&](const float (&kk)[EPL], const float (&vv)[EPL]) {
-      float sv[GRP];
-      score(kk, sv);
-      update(sv, vv);
     };
     for (int p0 = a; p0 < pend; p0 += TP) {
       const int np = min(TP, pend - p0);
       const int slot = rp.slot;
       wait_full(p, S, slot, rp.par);
-      const unsigned char *st = ring + static_cast<size_t>(slot) * STAGE_BYTES;
-      const uint16_t *kt = reinterpret_cast<const uint16_t *>(st) + lane * EPL;
+      const uint16_t *kt = reinterpret_cast<const uint16_t *>(ring + static_cast<size_t>(slot) * STAGE_BYTES);
       const uint16_t *vt = kt + static_cast<size_t>(np) * HD;
-      // two positions at a time: their scores' warp reductions overlap; the
-      // updates still run in position order (the same arithmetic as one by one)
-      int i = w;
-      for (; i + NCW < np; i += 2 * NCW) {
-        float kk[2][EPL], vv[2][EPL], sv[2][GRP];
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) {
-            kk[j][e] = bf2f(kt[static_cast<size_t>(i + j * NCW) * HD + e]);
-            vv[j][e] = bf2f(vt[static_cast<size_t>(i + j * NCW) * HD + e]);
-          }
-#pragma unroll
-        for (int j = 0; j < 2; ++j) score(kk[j], sv[j]);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) update(sv[j], vv[j]);
-      }
-      for (; i < np; i += NCW) {
-        float kk[EPL], vv[EPL];
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-          kk[e] = bf2f(kt[static_cast<size_t>(i) * HD + e]);
-          vv[e] = bf2f(vt[static_cast<size_t>(i) * HD + e]);
-        }
-        visit(kk, vv);
-      }
+      // warp w: positions 8w .. 8w+7 of every 8 * NCW
+      for (int j0 = 8 * w; j0 < np; j0 += 8 * NCW) block(kt + j0 * HD, vt + j0 * HD, min(8, np - j0));
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.empty[slot]);
       rp.next(p.stages);
     }
-    if (has_cur && w == NCW - 1) {
-      float kk[EPL], vv[EPL];
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) { kk[e] = S.kcur[lane * EPL + e]; vv[e] = S.vcur[lane * EPL + e]; }
-      visit(kk, vv);
-    }
+    if (has_cur && w == NCW - 1) block(S.kcur, S.vcur, 1);
 
     // ---- merge the 8 warps, then the chunks ---------------------------------
 #pragma unroll

@@ -174,7 +174,7 @@ struct SmemCtl {
   float bestv[NCW];
   int besti[NCW];
   float qs[MAX_GRP_HD];                  // normed, rotated, scaled queries of one unit
-  float kcur[128], vcur[128];            // this position's key / value (bf16-rounded)
+  uint16_t kcur[128], vcur[128];         // this position's key / value (bf16, as cached)
   float ow[NCW][MAX_GRP_HD];             // per-warp unnormalised attention outputs
   float mw[NCW][8], lw[NCW][8];          // per-warp running max / sum per head
   alignas(16) float xs[MAX_STAGE_K];     // staged GEMV input (fast layout 1)
