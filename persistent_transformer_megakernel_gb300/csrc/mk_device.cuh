@@ -861,13 +861,16 @@ __device__ __forceinline__ void gemv_fast_body(const Params &p, SmemCtl &S, unsi
         const int slot = rp.slot;
         wait_full(p, S, slot, rp.par);
         const unsigned char *st = ring + static_cast<size_t>(slot) * STAGE_BYTES;
-        // row slots past the tile's last row re-read that row and are zeroed
+        // row slots past the tile's last row re-read that row and are zeroed;
+        // a paired gate/up tile holds gate rows at 0.. and up rows at RT..
 #pragma unroll
         for (int i = 0; i < RPT; ++i) {
           const int row = rg + i * NG;
-          const int rr = min(row, rit - 1);
+          const bool paired = STAGED && RPT % 2 == 0 && kind == GV_GU;
+          const bool ok = paired ? (row < g.RT ? row < nr : row - g.RT < nr) : row < rit;
+          const int rr = paired ? row : min(row, rit - 1);
           const float dv = dot_chunked<KPT, CH, SPAN>(st + rr * rowb, kc, xr);
-          acc[b * RPT + i] = row < rit ? dv : 0.f;
+          acc[b * RPT + i] = ok ? dv : 0.f;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.empty[slot]);
@@ -897,6 +900,28 @@ __device__ __forceinline__ void gemv_fast_body(const Params &p, SmemCtl &S, unsi
               if (!isfinite(v)) set_err(p, MK_ERR_NUMERIC_D);
               if (v > best_v || (v == best_v && grow < best_i)) { best_v = v; best_i = grow; }
             }
+          }
+        }
+        continue;
+      }
+      if (RPT % 2 == 0 && kind == GV_GU) {
+        // gate row r of a tile is the warp's slot i < RPT/2, its up row (r +
+        // RT) slot i + RPT/2 of the same warp: the lane holding the gate sum
+        // takes the up sum by one shuffle and publishes SiLU(gate) * up
+        const float up = __shfl_down_sync(0xffffffffu, v, (RPT / 2) << (5 - LOGN));
+        const int sl = lane >> (5 - LOGN);
+        const int b = sl / RPT, i = sl % RPT;
+        const int ti = tb + b;
+        if ((lane & ((32 >> LOGN) - 1)) == 0 && i < RPT / 2 && ti < te) {
+          const int nr = min(g.RT, r1 - (r0 + ti * g.RT));
+          const int row = rg + i * NG;
+          if (row < nr) {
+            const int grow = r0 + ti * g.RT + row;
+            float y = 0.f, u = 0.f;   // the same additions as the shared-buffer epilogue
+            y += v;
+            u += up;
+            ll_store_rep(p, p.ll.u + static_cast<size_t>(layer) * p.I + ll_slot(p.geo[GV_DOWN], grow),
+                         y / (1.0f + expf(-y)) * u, tag);
           }
         }
         continue;
@@ -1408,7 +1433,7 @@ struct Producer {
       unsigned char *dst = claim(slot);
       if (!dst) return;
       const uint16_t *src[3];
-      uint32_t bytes[3];
+      uint32_t bytes[3], offs[3] = {0, 0, 0};
       int n = 0;
       if (kind == GV_QKV) {
         const int qr = p.Hq * p.d, kr = p.Hkv * p.d;
@@ -1426,6 +1451,10 @@ struct Producer {
         src[0] = S.layers[layer].w_gate + static_cast<size_t>(a) * g.K;
         src[1] = S.layers[layer].w_up + static_cast<size_t>(a) * g.K;
         bytes[0] = bytes[1] = static_cast<uint32_t>(nr) * rowb;
+        // up rows follow the gate rows; in the paired layout (staged, even
+        // rows per thread) always at row RT, so that a warp holds the gate and
+        // the up row of the same output in every tile, the last one included
+        offs[1] = (g.fast == 1 && g.RPTP % 2 == 0) ? static_cast<uint32_t>(g.RT) * rowb : bytes[0];
         n = 2;
       } else {
         const uint16_t *base = kind == GV_O ? S.layers[layer].wo
@@ -1440,8 +1469,8 @@ struct Producer {
       mbar_arrive_expect_tx(&S.full[slot], total);
       uint32_t off = 0;
       for (int i = 0; i < n; ++i) {
+        if (i > 0) off = kind == GV_GU ? offs[i] : off + bytes[i - 1];
         bulk_load(dst + off, src[i], bytes[i], &S.full[slot], pol_w);
-        off += bytes[i];
       }
       rp.next(p.stages);
     }
