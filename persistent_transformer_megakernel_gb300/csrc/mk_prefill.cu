@@ -23,6 +23,7 @@
 namespace mkp {
 
 constexpr int PF_THREADS = 256;
+constexpr int PF_MAXE = 16;                  // hidden <= PF_THREADS * PF_MAXE
 
 __device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 // round-to-nearest-even float -> bf16 bits (NaN kept quiet)
@@ -93,28 +94,49 @@ __global__ void pf_embed(const PfArgs a, int t0, int nt) {
 // h = x / sqrt(mean(x^2) + eps) * gain as three bf16 terms
 __global__ void pf_add_norm_split(const PfArgs a, const float *y, int ny, const uint16_t *gain, int t0, int nt,
                                   int hidden_layer) {
-  // y: ny split-K partials of the GEMM output, a.y_stride apart, or NULL
+  // y: ny split-K partials of the GEMM output, a.y_stride apart, or NULL.
+  // A thread's PF_MAXE elements stay in registers between the two passes, and
+  // every load of a pass is issued before its stores (one memory round trip
+  // per pass instead of one per element).
   __shared__ float red[PF_THREADS / 32];
   const int t = blockIdx.x;
   if (t >= nt) return;
   float *x = a.x + static_cast<size_t>(t) * a.H;
-  float ss = 0.f;
-  for (int k = threadIdx.x; k < a.H; k += blockDim.x) {
-    float v = x[k];
-    if (y) {
-      v = v + sum_parts(y, a.y_stride, ny, static_cast<size_t>(t) * a.H + k);
-      x[k] = v;
-      if (a.call->hidden && hidden_layer >= 0)
-        a.call->hidden[(static_cast<size_t>(t0 + t) * (a.L + 1) + hidden_layer) * a.H + k] = v;
+  float *hid = (y && a.call->hidden && hidden_layer >= 0)
+                   ? a.call->hidden + (static_cast<size_t>(t0 + t) * (a.L + 1) + hidden_layer) * a.H
+                   : nullptr;
+  float v[PF_MAXE];
+#pragma unroll
+  for (int i = 0; i < PF_MAXE; ++i) {
+    const int k = threadIdx.x + i * PF_THREADS;
+    v[i] = 0.f;
+    if (k < a.H) {
+      v[i] = x[k];
+      if (y) v[i] = v[i] + sum_parts(y, a.y_stride, ny, static_cast<size_t>(t) * a.H + k);
     }
-    ss = fmaf(v, v, ss);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < PF_MAXE; ++i) {
+    const int k = threadIdx.x + i * PF_THREADS;
+    if (k < a.H) {
+      if (y) {
+        x[k] = v[i];
+        if (hid) hid[k] = v[i];
+      }
+      ss = fmaf(v[i], v[i], ss);
+    }
   }
   const float tot = block_sum(ss, red);
   const float rs = 1.0f / sqrtf(tot / static_cast<float>(a.H) + a.eps);
   const size_t o = static_cast<size_t>(t) * a.H;
-  for (int k = threadIdx.x; k < a.H; k += blockDim.x) {
-    const float h = x[k] * rs * bf2f(gain[k]);
-    split3(h, a.hs[o + k], a.hs[a.hs_stride + o + k], a.hs[2 * a.hs_stride + o + k]);
+#pragma unroll
+  for (int i = 0; i < PF_MAXE; ++i) {
+    const int k = threadIdx.x + i * PF_THREADS;
+    if (k < a.H) {
+      const float h = v[i] * rs * bf2f(gain[k]);
+      split3(h, a.hs[o + k], a.hs[a.hs_stride + o + k], a.hs[2 * a.hs_stride + o + k]);
+    }
   }
 }
 
@@ -556,6 +578,7 @@ int pf_init(PfState &st, int tc, int H, int Hq, int Hkv, int d, int I) {
   if (st.tc >= tc) return MK_OK;
   pf_free(st);
   if (H % 64 || (Hq * d) % 64 || I % 64) return MK_ERR_UNSUPPORTED;   // GEMM K blocks of 64
+  if (H > PF_THREADS * PF_MAXE) return MK_ERR_UNSUPPORTED;           // pf_add_norm_split's registers
   const size_t rows = static_cast<size_t>(Hq + 2 * Hkv) * d;
   size_t kmax = H;
   if (static_cast<size_t>(Hq) * d > kmax) kmax = static_cast<size_t>(Hq) * d;
