@@ -1247,13 +1247,16 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
     }
     // positions j < nv of rows kb + j * HD (keys) and vb + j * HD (values)
     auto block = [&](const uint16_t *kb, const uint16_t *vb, int nv) {
-      float sp[NSL];
+      float sp[NSL], vv[8][EPL];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int jj = min(j, nv - 1);        // past the last position: re-read it, masked below
         float kk[EPL];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) kk[e] = bf2f(kb[jj * HD + lane * EPL + e]);
+        for (int e = 0; e < EPL; ++e) {
+          kk[e] = bf2f(kb[jj * HD + lane * EPL + e]);
+          vv[j][e] = bf2f(vb[jj * HD + lane * EPL + e]);
+        }
 #pragma unroll
         for (int h = 0; h < GRP; ++h) {
           float x = 0.f;
@@ -1290,9 +1293,8 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float pj = __shfl_sync(0xffffffffu, pe, (h * 8 + j) << LPS);
-          const int jj = min(j, nv - 1);      // value rows read where they are used (fewer live registers)
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) o[h][e] = fmaf(pj, bf2f(vb[jj * HD + lane * EPL + e]), o[h][e]);
+          for (int e = 0; e < EPL; ++e) o[h][e] = fmaf(pj, vv[j][e], o[h][e]);
         }
       }
     };
