@@ -17,6 +17,11 @@
 // Operands follow the 128-byte swizzled layouts of csrc/mk_tc.cuh: Q, K and P
 // K-major, V MN-major (positions x head_dim, as the cache holds it).
 //
+// Long prompts split the cached positions of a query tile over gridDim.z
+// CTAs (blockIdx.z takes tiles [z * tps, (z + 1) * tps)); each writes its
+// unnormalised output with its rows' maximum and sum, and pf_attn_merge
+// combines the splits.
+//
 // Warp roles (352 threads): softmax warps 0-7, warp w owning TMEM lanes
 // 32 (w % 4) .. + 31 (one query row per thread) and columns 32 (w / 4) .. + 31
 // of every 64-position tile; warp 8 lane 0 issues the TMA loads of K and V
@@ -136,7 +141,25 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   const int ntok = min(TT, nt - tok0);
   const int base_pos = a.call->pos0 + t0;
   const int pmax = base_pos + tok0 + ntok - 1;          // the CTA's last cached slot
-  const int nT = pmax / AT_POS + 1;                     // tiles per pass
+  // position split z: tiles [jb, jb + nT) of this query tile's 0 .. pmax / AT_POS
+  const int ns = gridDim.z;
+  const int tps = ns > 1 ? ((base_pos + nt - 1) / AT_POS + ns) / ns : 0;   // the chunk's tiles / ns, rounded up
+  const int jb = ns > 1 ? static_cast<int>(blockIdx.z) * tps : 0;
+  const int nT = ns > 1 ? max(0, min(pmax / AT_POS + 1, jb + tps) - jb) : pmax / AT_POS + 1;   // tiles per pass
+  const int qrows = a.Hq * HD;
+  if (nT == 0) {
+    // no cached position of this split reaches these rows: an empty state (l = 0)
+    if (threadIdx.x < AT_ROWS) {
+      const int r = threadIdx.x, tt = r / GRP, h = r % GRP;
+      if (tt < ntok) {
+        float *dst = a.attn_part + ((static_cast<size_t>(blockIdx.z) * nt + tok0 + tt) * a.Hq + g * GRP + h) * (HD + 2);
+        dst[HD] = -INFINITY;
+        dst[HD + 1] = 0.f;
+      }
+    }
+    return;
+  }
+  (void)qrows;
   const int rows = (a.Hq + 2 * a.Hkv) * HD;
   const int kv_row0 = (layer * a.Hkv + g) * a.max_seq;  // first cache row of (layer, g)
 
@@ -199,7 +222,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         mbar_expect_tx(&kfull[kb], LY::KV_TILE);
 #pragma unroll
         for (int at = 0; at < LY::ATOMS; ++at)
-          tma_load_2d_hint(Ks + kb * LY::KV_TILE + at * (AT_POS * 128), &tk, at * 64, kv_row0 + j * AT_POS,
+          tma_load_2d_hint(Ks + kb * LY::KV_TILE + at * (AT_POS * 128), &tk, at * 64, kv_row0 + (jb + j) * AT_POS,
                            &kfull[kb], keep);
         ++nk;
         if (u >= nT) {
@@ -211,7 +234,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           mbar_expect_tx(&vfull[vb], LY::KV_TILE);
 #pragma unroll
           for (int at = 0; at < LY::ATOMS; ++at)
-            tma_load_2d_hint(Vs + vb * LY::KV_TILE + at * (AT_POS * 128), &tv, at * 64, kv_row0 + j * AT_POS,
+            tma_load_2d_hint(Vs + vb * LY::KV_TILE + at * (AT_POS * 128), &tv, at * 64, kv_row0 + (jb + j) * AT_POS,
                              &vfull[vb], keep);
           ++nv;
         }
@@ -302,7 +325,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         tmem_ld16(tl + static_cast<uint32_t>(sb * AT_POS + col), v);
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          if (u * AT_POS + col + i <= prow) m = fmaxf(m, v[i]);
+          if ((jb + u) * AT_POS + col + i <= prow) m = fmaxf(m, v[i]);
       }
       tc_fence_before();
       __syncwarp();
@@ -336,7 +359,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int c = col + half * 8 + e;
-            pv[e] = (j * AT_POS + c <= prow) ? __expf(v[half * 8 + e] - m) : 0.f;
+            pv[e] = ((jb + j) * AT_POS + c <= prow) ? __expf(v[half * 8 + e] - m) : 0.f;
           }
           uint4 t0, t1, t2;
           split3x8(pv, t0, t1, t2);
@@ -366,18 +389,24 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     if (!done) {
       if (lane == 0) atomicCAS(a.err, 0, MK_ERR_TIMEOUT);
     } else if (ok) {
-      const float inv = 1.0f / l;
+      // one split: o = O / l; several: this split's O with the row's m and l
+      const float inv = ns > 1 ? 1.0f : 1.0f / l;
       const int h = r % GRP;
-      float *dst = a.attn + static_cast<size_t>(tok0 + tt) * a.Hq * HD + static_cast<size_t>(g * GRP + h) * HD;
+      float *dst = ns > 1 ? a.attn_part + ((static_cast<size_t>(blockIdx.z) * nt + tok0 + tt) * a.Hq + g * GRP + h) *
+                                              (HD + 2)
+                          : a.attn + static_cast<size_t>(tok0 + tt) * a.Hq * HD + static_cast<size_t>(g * GRP + h) * HD;
+      if (ns > 1 && hf == 0 && tt < ntok) {
+        dst[HD] = l > 0.f ? m : -INFINITY;
+        dst[HD + 1] = l;
+      }
 #pragma unroll 1
       for (int c0 = hf * (HD / 2); c0 < (hf + 1) * (HD / 2); c0 += 16) {
         float v[16];
         tmem_ld16(tl + static_cast<uint32_t>(2 * AT_POS + c0), v);
         if (tt < ntok) {
 #pragma unroll
-          for (int i = 0; i < 16; i += 4)
-            *reinterpret_cast<float4 *>(dst + c0 + i) =
-                make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
+          for (int i = 0; i < 16; i += 2)
+            *reinterpret_cast<float2 *>(dst + c0 + i) = make_float2(v[i] * inv, v[i + 1] * inv);
         }
       }
     }
@@ -385,6 +414,36 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 9) tmem_dealloc(tbase, LY::TMEM_COLS);
+}
+
+// The position splits of one (token, q head): o = sum_s e^(m_s - M) O_s /
+// sum_s e^(m_s - M) l_s with M the largest m_s of the non-empty splits, in
+// split order.  One warp per (token, head), lane l dims l, l + 32, ...
+template <int HD>
+__global__ void pf_attn_merge(const PfArgs a, int nt, int ns) {
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (wid >= nt * a.Hq) return;
+  const int tok = wid / a.Hq, head = wid - tok * a.Hq;
+  const size_t stride = static_cast<size_t>(nt) * a.Hq * (HD + 2);
+  const float *src = a.attn_part + (static_cast<size_t>(tok) * a.Hq + head) * (HD + 2);
+  float M = -INFINITY;
+  for (int z = 0; z < ns; ++z)
+    if (src[z * stride + HD + 1] > 0.f) M = fmaxf(M, src[z * stride + HD]);
+  float L = 0.f, o[HD / 32];
+#pragma unroll
+  for (int k = 0; k < HD / 32; ++k) o[k] = 0.f;
+  for (int z = 0; z < ns; ++z) {
+    const float lz = src[z * stride + HD + 1];
+    if (lz > 0.f) {
+      const float w = expf(src[z * stride + HD] - M);
+      L = fmaf(w, lz, L);
+#pragma unroll
+      for (int k = 0; k < HD / 32; ++k) o[k] = fmaf(w, src[z * stride + lane + 32 * k], o[k]);
+    }
+  }
+  float *dst = a.attn + (static_cast<size_t>(tok) * a.Hq + head) * HD;
+#pragma unroll
+  for (int k = 0; k < HD / 32; ++k) dst[lane + 32 * k] = o[k] / L;
 }
 
 // ---------------------------------------------------------------------------
@@ -405,8 +464,15 @@ int launch_tc(const CUtensorMap &tk, const CUtensorMap &tv, const PfArgs &a, int
     attr = true;
   }
   constexpr int TT = AT_ROWS / GRP;
-  pf_attn_tc<HD, GRP><<<dim3((nt + TT - 1) / TT, a.Hkv), AT_THREADS, AttnLayout<HD>::SMEM, s>>>(tk, tv, a, layer,
-                                                                                                  t0, nt);
+  // prompts reaching past PF_ATTN_SPLIT_MIN positions (from the chunk's first
+  // token at slot pos0 = 0) split their positions over PF_ATTN_SPLITS CTAs
+  const int ns = (t0 + nt > PF_ATTN_SPLIT_MIN) ? PF_ATTN_SPLITS : 1;
+  pf_attn_tc<HD, GRP><<<dim3((nt + TT - 1) / TT, a.Hkv, ns), AT_THREADS, AttnLayout<HD>::SMEM, s>>>(tk, tv, a, layer,
+                                                                                                      t0, nt);
+  if (ns > 1) {
+    const int warps = nt * a.Hq;
+    pf_attn_merge<HD><<<(warps + 7) / 8, 256, 0, s>>>(a, nt, ns);
+  }
   return cudaGetLastError() == cudaSuccess ? MK_OK : MK_ERR_CUDA;
 }
 

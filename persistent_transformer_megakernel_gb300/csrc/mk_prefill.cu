@@ -23,7 +23,6 @@
 namespace mkp {
 
 constexpr int PF_THREADS = 256;
-constexpr int PF_MAXE = 16;                  // hidden <= PF_THREADS * PF_MAXE
 
 __device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 // round-to-nearest-even float -> bf16 bits (NaN kept quiet)
@@ -94,49 +93,28 @@ __global__ void pf_embed(const PfArgs a, int t0, int nt) {
 // h = x / sqrt(mean(x^2) + eps) * gain as three bf16 terms
 __global__ void pf_add_norm_split(const PfArgs a, const float *y, int ny, const uint16_t *gain, int t0, int nt,
                                   int hidden_layer) {
-  // y: ny split-K partials of the GEMM output, a.y_stride apart, or NULL.
-  // A thread's PF_MAXE elements stay in registers between the two passes, and
-  // every load of a pass is issued before its stores (one memory round trip
-  // per pass instead of one per element).
+  // y: ny split-K partials of the GEMM output, a.y_stride apart, or NULL
   __shared__ float red[PF_THREADS / 32];
   const int t = blockIdx.x;
   if (t >= nt) return;
   float *x = a.x + static_cast<size_t>(t) * a.H;
-  float *hid = (y && a.call->hidden && hidden_layer >= 0)
-                   ? a.call->hidden + (static_cast<size_t>(t0 + t) * (a.L + 1) + hidden_layer) * a.H
-                   : nullptr;
-  float v[PF_MAXE];
-#pragma unroll
-  for (int i = 0; i < PF_MAXE; ++i) {
-    const int k = threadIdx.x + i * PF_THREADS;
-    v[i] = 0.f;
-    if (k < a.H) {
-      v[i] = x[k];
-      if (y) v[i] = v[i] + sum_parts(y, a.y_stride, ny, static_cast<size_t>(t) * a.H + k);
-    }
-  }
   float ss = 0.f;
-#pragma unroll
-  for (int i = 0; i < PF_MAXE; ++i) {
-    const int k = threadIdx.x + i * PF_THREADS;
-    if (k < a.H) {
-      if (y) {
-        x[k] = v[i];
-        if (hid) hid[k] = v[i];
-      }
-      ss = fmaf(v[i], v[i], ss);
+  for (int k = threadIdx.x; k < a.H; k += blockDim.x) {
+    float v = x[k];
+    if (y) {
+      v = v + sum_parts(y, a.y_stride, ny, static_cast<size_t>(t) * a.H + k);
+      x[k] = v;
+      if (a.call->hidden && hidden_layer >= 0)
+        a.call->hidden[(static_cast<size_t>(t0 + t) * (a.L + 1) + hidden_layer) * a.H + k] = v;
     }
+    ss = fmaf(v, v, ss);
   }
   const float tot = block_sum(ss, red);
   const float rs = 1.0f / sqrtf(tot / static_cast<float>(a.H) + a.eps);
   const size_t o = static_cast<size_t>(t) * a.H;
-#pragma unroll
-  for (int i = 0; i < PF_MAXE; ++i) {
-    const int k = threadIdx.x + i * PF_THREADS;
-    if (k < a.H) {
-      const float h = v[i] * rs * bf2f(gain[k]);
-      split3(h, a.hs[o + k], a.hs[a.hs_stride + o + k], a.hs[2 * a.hs_stride + o + k]);
-    }
+  for (int k = threadIdx.x; k < a.H; k += blockDim.x) {
+    const float h = x[k] * rs * bf2f(gain[k]);
+    split3(h, a.hs[o + k], a.hs[a.hs_stride + o + k], a.hs[2 * a.hs_stride + o + k]);
   }
 }
 
@@ -578,7 +556,6 @@ int pf_init(PfState &st, int tc, int H, int Hq, int Hkv, int d, int I) {
   if (st.tc >= tc) return MK_OK;
   pf_free(st);
   if (H % 64 || (Hq * d) % 64 || I % 64) return MK_ERR_UNSUPPORTED;   // GEMM K blocks of 64
-  if (H > PF_THREADS * PF_MAXE) return MK_ERR_UNSUPPORTED;           // pf_add_norm_split's registers
   const size_t rows = static_cast<size_t>(Hq + 2 * Hkv) * d;
   size_t kmax = H;
   if (static_cast<size_t>(Hq) * d > kmax) kmax = static_cast<size_t>(Hq) * d;
@@ -592,6 +569,7 @@ int pf_init(PfState &st, int tc, int H, int Hq, int Hkv, int d, int I) {
   const size_t T = tc;
   int rc;
   if ((rc = dalloc(&st.x, T * H)) || (rc = dalloc(&st.qkv, T * rows)) || (rc = dalloc(&st.attn, T * Hq * d)) ||
+      (rc = dalloc(&st.attn_part, static_cast<size_t>(PF_ATTN_SPLITS) * T * Hq * (d + 2))) ||
       (rc = dalloc(&st.qkv_p, PF_SPLITS_WIDE * T * rows)) || (rc = dalloc(&st.y_p, PF_SPLITS_NARROW * T * H)) ||
       (rc = dalloc(&st.gu_p, PF_SPLITS_WIDE * T * 2 * I)) ||
       (rc = dalloc(&st.hs, 3 * T * kmax)) || (rc = dalloc(&st.pv, T * PF_ARGMAX_BLOCKS)) ||
@@ -630,7 +608,7 @@ void pf_free(PfState &st) {
     cudaGraphDestroy(g.graph);
   }
   if (st.cap) cudaStreamDestroy(st.cap);
-  void *ps[] = {st.x, st.qkv, st.attn, st.qkv_p, st.y_p, st.gu_p, st.logits, st.pv, st.pi, st.hs, st.err, st.call};
+  void *ps[] = {st.x, st.qkv, st.attn, st.attn_part, st.qkv_p, st.y_p, st.gu_p, st.logits, st.pv, st.pi, st.hs, st.err, st.call};
   for (void *p : ps)
     if (p) cudaFree(p);
   st = PfState();
@@ -754,7 +732,7 @@ int pf_run(PfState &st, PfArgs a, const PfLayer *layers, const uint16_t *final_n
   }
   if (!st.kv_maps) st.kv_maps = attn_tc_maps(a, &st.kmap, &st.vmap);
   const int rows = (a.Hq + 2 * a.Hkv) * a.d;
-  a.x = st.x; a.qkv = st.qkv; a.attn = st.attn;
+  a.x = st.x; a.qkv = st.qkv; a.attn = st.attn; a.attn_part = st.attn_part;
   a.qkv_p = st.qkv_p; a.qkv_stride = T * rows;
   a.y_p = st.y_p; a.y_stride = T * a.H;
   a.hs = st.hs; a.hs_stride = T * st.kmax;

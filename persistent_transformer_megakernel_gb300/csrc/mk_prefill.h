@@ -42,6 +42,7 @@ struct PfArgs {
   const PfCall *call;               // device copy of the call's fields
   int *err;                         // first error code (device)
   float *x, *qkv, *attn;            // chunk scratch (fp32): residual, normed q, attention output
+  float *attn_part;                 // split-KV attention partials [PF_ATTN_SPLITS][tc][Hq][d + 2] (o, m, l)
   float *qkv_p, *y_p;               // GEMM outputs as split-K partials, qkv_stride / y_stride apart
   size_t qkv_stride, y_stride;
   int qkv_n;                        // partials of the QKV output of the current chunk
@@ -57,6 +58,9 @@ struct PfLayer {
 // split-K partials the scratch holds per GEMM output (QKV and gate / up; O and down)
 constexpr int PF_SPLITS_WIDE = 4;
 constexpr int PF_SPLITS_NARROW = 8;
+// position splits of one query tile's cached positions (long prompts: more CTAs per layer)
+constexpr int PF_ATTN_SPLITS = 4;
+constexpr int PF_ATTN_SPLIT_MIN = 512;   // chunks ending past this many prompt positions split
 // captured prefill graphs kept per handle (least recently used replaced)
 constexpr int PF_MAX_GRAPHS = 8;
 
@@ -64,7 +68,7 @@ constexpr int PF_MAX_GRAPHS = 8;
 struct PfState {
   int tc = 0;                       // tokens per chunk the scratch holds
   int sms = 0;                      // multiprocessors (split-K sizing)
-  float *x = nullptr, *qkv = nullptr, *attn = nullptr;
+  float *x = nullptr, *qkv = nullptr, *attn = nullptr, *attn_part = nullptr;
   float *qkv_p = nullptr, *y_p = nullptr;  // [splits][tc][N] GEMM partials
   float *gu_p = nullptr;            // [splits][tc][2 I]: gate columns, then up columns
   float *logits = nullptr;          // [logit_rows][V], allocated on the first LM head

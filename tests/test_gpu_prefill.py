@@ -70,6 +70,8 @@ def _prefill_then_decode(name, T, n_steps, max_seq, pos3_mode=None, sentinel=Fal
     ("tiny", 300, 4, 320),      # two chunks of the 256-token scratch
     ("mha", 70, 6, 96),         # group 1, head_dim 128: three query tiles, two cache tiles
     ("mha64", 100, 4, 128),     # group 1, head_dim 64, ragged last query tile
+    ("mid", 700, 4, 720),       # the third chunk ends past 512 positions: positions split over 4 CTAs + merge
+    ("gqa4", 600, 3, 640),      # the same with group 4, head_dim 64
 ])
 def test_prefill_parity(name, T, n_steps, max_seq):
     _prefill_then_decode(name, T, n_steps, max_seq)
