@@ -1168,7 +1168,7 @@ static __device__ __noinline__ void merge_ticket_chunks(const Params &p, unsigne
   }
 }
 
-template <int HD, int GRP>
+template <int HD, int GRP, bool BLOCKS = true>
 __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring, int l, int f, int cta,
                                 unsigned tag, RingPos &rp, int gp, const AttnSched &as) {
   constexpr int EPL = HD / 32;
@@ -1229,14 +1229,6 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
     cons_sync();
     trace_mark(p, gp, cta, 1);
 
-    // ---- scores and online softmax, 8 positions per warp at a time -----------
-    // Lane l holds dims l*EPL .. l*EPL+EPL-1 of q, of every key and value row
-    // and of the output.  A block of 8 positions: per-lane partial scores of
-    // the 8 x GRP (head, position) pairs, one multi-slot warp reduction (lane
-    // holds slot (h * 8 + j) after it), the block's maximum and sum per head
-    // by shuffles among the lanes of a head, then the rescaled output update.
-    constexpr int NSL = 8 * GRP;
-    constexpr int LPS = NSL >= 32 ? 0 : NSL >= 16 ? 1 : NSL >= 8 ? 2 : 3;   // log2 lanes per slot
     float q[GRP][EPL], o[GRP][EPL], m[GRP], ls[GRP];
 #pragma unroll
     for (int h = 0; h < GRP; ++h) {
@@ -1245,6 +1237,15 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
       m[h] = -INFINITY;
       ls[h] = 0.f;
     }
+    if constexpr (BLOCKS) {
+    // ---- scores and online softmax, 8 positions per warp at a time -----------
+    // Lane l holds dims l*EPL .. l*EPL+EPL-1 of q, of every key and value row
+    // and of the output.  A block of 8 positions: per-lane partial scores of
+    // the 8 x GRP (head, position) pairs, one multi-slot warp reduction (lane
+    // holds slot (h * 8 + j) after it), the block's maximum and sum per head
+    // by shuffles among the lanes of a head, then the rescaled output update.
+    constexpr int NSL = 8 * GRP;
+    constexpr int LPS = NSL >= 32 ? 0 : NSL >= 16 ? 1 : NSL >= 8 ? 2 : 3;   // log2 lanes per slot
     // positions j < nv of rows kb + j * HD (keys) and vb + j * HD (values)
     auto block = [&](const uint16_t *kb, const uint16_t *vb, int nv) {
       float sp[NSL], vv[8][EPL];
@@ -1311,6 +1312,82 @@ __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring
       rp.next(p.stages);
     }
     if (has_cur && w == NCW - 1) block(S.kcur, S.vcur, 1);
+
+    } else {
+    // ---- (!BLOCKS) scores and online softmax, one warp per position ----------
+    // score of one cached position for every head of the group (warp-reduced)
+    auto score = [&](const float (&kk)[EPL], float (&sv)[GRP]) {
+#pragma unroll
+      for (int h = 0; h < GRP; ++h) {
+        float x = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) x = fmaf(q[h][e], kk[e], x);
+        sv[h] = warp_sum(x);
+      }
+    };
+    // online-softmax update with one position's scores and value row
+    auto update = [&](const float (&sv)[GRP], const float (&vv)[EPL]) {
+#pragma unroll
+      for (int h = 0; h < GRP; ++h) {
+        const float mn = fmaxf(m[h], sv[h]);
+        const float sc = expf(m[h] - mn);
+        const float pe = expf(sv[h] - mn);
+        ls[h] = ls[h] * sc + pe;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[h][e] = fmaf(pe, vv[e], o[h][e] * sc);
+        m[h] = mn;
+      }
+    };
+    auto visit = [&](const float (&kk)[EPL], const float (&vv)[EPL]) {
+      float sv[GRP];
+      score(kk, sv);
+      update(sv, vv);
+    };
+    for (int p0 = a; p0 < pend; p0 += TP) {
+      const int np = min(TP, pend - p0);
+      const int slot = rp.slot;
+      wait_full(p, S, slot, rp.par);
+      const unsigned char *st = ring + static_cast<size_t>(slot) * STAGE_BYTES;
+      const uint16_t *kt = reinterpret_cast<const uint16_t *>(st) + lane * EPL;
+      const uint16_t *vt = kt + static_cast<size_t>(np) * HD;
+      // two positions at a time: their scores' warp reductions overlap; the
+      // updates still run in position order (the same arithmetic as one by one)
+      int i = w;
+      for (; i + NCW < np; i += 2 * NCW) {
+        float kk[2][EPL], vv[2][EPL], sv[2][GRP];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) {
+            kk[j][e] = bf2f(kt[static_cast<size_t>(i + j * NCW) * HD + e]);
+            vv[j][e] = bf2f(vt[static_cast<size_t>(i + j * NCW) * HD + e]);
+          }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) score(kk[j], sv[j]);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) update(sv[j], vv[j]);
+      }
+      for (; i < np; i += NCW) {
+        float kk[EPL], vv[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          kk[e] = bf2f(kt[static_cast<size_t>(i) * HD + e]);
+          vv[e] = bf2f(vt[static_cast<size_t>(i) * HD + e]);
+        }
+        visit(kk, vv);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[slot]);
+      rp.next(p.stages);
+    }
+    if (has_cur && w == NCW - 1) {
+      float kk[EPL], vv[EPL];
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) { kk[e] = bf2f(S.kcur[lane * EPL + e]); vv[e] = bf2f(S.vcur[lane * EPL + e]); }
+      visit(kk, vv);
+    }
+
+    }
 
     // ---- merge the 8 warps, then the chunks ---------------------------------
 #pragma unroll
@@ -1728,7 +1805,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mk_decode_kernel(const __grid_con
       switch (k) {
         case 0: gemv_run<PL, GV_QKV>(p, S, ring, l, f, cta, in_id, tag, st, gp); break;
         case 1:
-          if constexpr (PL::fixed) attention_phase<HD, PL::grp>(p, S, ring, l, f, cta, tag, rp, gp, as);
+          if constexpr (PL::fixed) attention_phase<HD, PL::grp, PL::attn_blocks>(p, S, ring, l, f, cta, tag, rp, gp, as);
           else attention_dispatch<HD>(p, S, ring, l, f, cta, tag, rp, gp, as);
           break;
         case 2: gemv_run<PL, GV_O>(p, S, ring, l, f, cta, in_id, tag, st, gp); break;

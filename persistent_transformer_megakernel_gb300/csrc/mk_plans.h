@@ -18,6 +18,7 @@ struct PlanHidden1024 {
   // dims, which the TTS talker mirrors): any vocabulary
   static constexpr bool fixed = true;
   static constexpr int hd = 128, grp = 2;
+  static constexpr bool attn_blocks = true;     // attention in 8-position blocks per warp
   static constexpr int spec[5][4] = {{1, 32, 2, 2}, {2, 8, 8, 1}, {1, 32, 2, 2}, {2, 12, 4, 2}, {1, 32, 2, 2}};
 };
 
@@ -25,12 +26,14 @@ struct PlanHidden2048 {
   // hidden 2048, 16 query / 8 KV heads of 128, MLP 6144 (the Qwen3-1.7B dims)
   static constexpr bool fixed = true;
   static constexpr int hd = 128, grp = 2;
+  static constexpr bool attn_blocks = false;    // one position per warp (measured 4% faster at this shape)
   static constexpr int spec[5][4] = {{1, 64, 1, 4}, {2, 8, 8, 2}, {1, 64, 1, 4}, {2, 24, 2, 8}, {1, 64, 1, 4}};
 };
 
 struct PlanGeneral {
   static constexpr bool fixed = false;
   static constexpr int hd = 0, grp = 0;
+  static constexpr bool attn_blocks = true;
   static constexpr int spec[5][4] = {};
 };
 
