@@ -518,7 +518,8 @@ def run_gpu(args, rank, world):
                      "frac": achieved / peak, "traffic": measured_traffic(args.workload, n_timed),
                      "peak_source": "%s hbm_gbs (copy bandwidth)" % peak_src,
                      "algorithmic_bytes_per_launch": bytes_launch,
-                     "kernel": "mk::mk_decode_kernel<%d>" % s["head_dim"]},
+                     "kernel": "mk::mk_decode_kernel<%d, %s>" % (
+                         s["head_dim"], {1: "PlanHidden1024", 2: "PlanHidden2048"}.get(info.get("plan", 0), "PlanGeneral"))},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "e2e": e2e,
