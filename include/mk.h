@@ -286,6 +286,16 @@ int mk_decode_host(mk_handle *h, const int32_t *h_in_ids, int32_t n_in, int32_t 
  * TTS?", measures the kernel's bandwidth use by).  MK_ERR_INVALID_ARG on NULL. */
 int mk_get_info(const mk_handle *h, mk_info *info);
 
+/* The decode kernel mk_create would pick for this shape on a device with n_sm
+ * multiprocessors (one CTA each), as mk_info.plan: 0 the general kernel, 1 the
+ * one compiled for hidden 1024 / MLP 3072 / 16:8 heads of 128, 2 the one for
+ * hidden 2048 / MLP 6144 / 16:8 heads of 128.  Runs the same shape checks and
+ * layout choice as mk_create, needs no device and allocates nothing (the
+ * compiled instantiations are an implementation choice; the pages have no
+ * counterpart of this call).  Errors: MK_ERR_INVALID_ARG (NULL pointers,
+ * n_sm < 1, a config mk_create rejects as invalid), MK_ERR_UNSUPPORTED. */
+int mk_plan_for(const mk_config *cfg, int32_t n_sm, int32_t *plan);
+
 /* Talker input rows: out[r] = sum_{j<n_books} books[j][codes[r][j]] + text[text_ids[r]],
  * accumulated in fp32 in table order (page B, "Why Does a Single Kernel Even
  * Matter for TTS?": each talker input is the sum of the 16 codebook embeddings

@@ -14,4 +14,5 @@ from ._binding import (  # noqa: F401
     error_string,
     lib_path,
     load_library,
+    plan_for,
 )

@@ -71,7 +71,7 @@ class mk_info(C.Structure):
 #: every symbol include/mk.h declares
 EXPORTS = ("mk_create", "mk_reset_kv", "mk_decode", "mk_prefill", "mk_decode_start", "mk_decode_wait",
            "mk_mailbox_read", "mk_decode_host", "mk_get_info", "mk_embed_sum",
-           "mk_embed_sum_noalloc", "mk_destroy", "mk_error_string")
+           "mk_embed_sum_noalloc", "mk_destroy", "mk_error_string", "mk_plan_for")
 
 _lib = None
 
@@ -99,6 +99,7 @@ def load_library(path: Optional[str] = None):
     lib.mk_mailbox_read.argtypes = [vp, vp, i32, C.POINTER(i32)]
     lib.mk_decode_host.argtypes = [vp, vp, i32, i32, vp, C.POINTER(mk_decode_opts), vp]
     lib.mk_get_info.argtypes = [vp, C.POINTER(mk_info)]
+    lib.mk_plan_for.argtypes = [C.POINTER(mk_config), i32, C.POINTER(i32)]
     lib.mk_embed_sum.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, i32, vp, vp]
     lib.mk_embed_sum_noalloc.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, i32, vp, vp]
     lib.mk_destroy.argtypes = [vp]
@@ -230,6 +231,31 @@ def check_weights(shape: dict, weights: dict, device=None) -> None:
             one(lw[k], "layers[%d].%s" % (l, k), shp)
 
 
+def config_struct(s: dict, max_seq: int, rope_positions: int = 0) -> mk_config:
+    """The ``mk_config`` of a shape dict (``workloads.shape``)."""
+    cfg = mk_config()
+    cfg.n_layers, cfg.hidden = s["n_layers"], s["hidden"]
+    cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim = s["n_q_heads"], s["n_kv_heads"], s["head_dim"]
+    cfg.intermediate, cfg.vocab, cfg.vocab_in = s["intermediate"], s["vocab"], s["vocab_in"]
+    cfg.rms_eps, cfg.rope_theta = s.get("rms_eps", 1e-6), s.get("rope_theta", 1e6)
+    ms = s.get("mrope_sections")
+    cfg.rope_mode = 0 if ms is None else (2 if s.get("mrope_interleaved") else 1)
+    if ms is not None:
+        cfg.mrope_sections[0], cfg.mrope_sections[1], cfg.mrope_sections[2] = ms
+    cfg.max_seq, cfg.rope_positions, cfg.flags = max_seq, rope_positions, 0
+    return cfg
+
+
+def plan_for(s: dict, n_sm: int, max_seq: int = 4096) -> int:
+    """``mk_plan_for``: the decode kernel mk_create picks for shape ``s`` on a
+    device with ``n_sm`` multiprocessors (0 general, 1 / 2 the kernels compiled
+    for the 0.6B / 1.7B dims).  Needs no device."""
+    lib = load_library()
+    plan = C.c_int32(-1)
+    _check(lib.mk_plan_for(C.byref(config_struct(s, max_seq)), int(n_sm), C.byref(plan)), "mk_plan_for")
+    return plan.value
+
+
 def _dev_bf16(bits: np.ndarray, device) -> torch.Tensor:
     t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
     return t.to(device, non_blocking=False).contiguous()
@@ -273,16 +299,7 @@ class Decoder:
         for l, lw in enumerate(weights["layers"]):
             for k in mk_layer_weights._fields_:
                 setattr(self._layers[l], k[0], dev(lw[k[0]]).data_ptr())
-        cfg = mk_config()
-        cfg.n_layers, cfg.hidden = L, s["hidden"]
-        cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim = s["n_q_heads"], s["n_kv_heads"], s["head_dim"]
-        cfg.intermediate, cfg.vocab, cfg.vocab_in = s["intermediate"], s["vocab"], s["vocab_in"]
-        cfg.rms_eps, cfg.rope_theta = s.get("rms_eps", 1e-6), s.get("rope_theta", 1e6)
-        ms = s.get("mrope_sections")
-        cfg.rope_mode = 0 if ms is None else (2 if s.get("mrope_interleaved") else 1)
-        if ms is not None:
-            cfg.mrope_sections[0], cfg.mrope_sections[1], cfg.mrope_sections[2] = ms
-        cfg.max_seq, cfg.rope_positions, cfg.flags = max_seq, rope_positions, 0
+        cfg = config_struct(s, max_seq, rope_positions)
         w = mk_weights()
         w.embed = self.embed.data_ptr()
         w.lm_head = None if self.lm_head is None else self.lm_head.data_ptr()

@@ -129,9 +129,15 @@ bool plan_matches(int d, int grp, const mk::GemvGeom *geo) {
   }
   return true;
 }
-const void *pick_kernel(int d, int grp, const mk::GemvGeom *geo) {
-  if (plan_matches<mk::PlanHidden1024>(d, grp, geo)) return mk::kernel_hidden1024();
-  if (plan_matches<mk::PlanHidden2048>(d, grp, geo)) return mk::kernel_hidden2048();
+// plan id (mk_info.plan): 1 PlanHidden1024, 2 PlanHidden2048, 0 the general kernel
+int pick_plan(int d, int grp, const mk::GemvGeom *geo) {
+  if (plan_matches<mk::PlanHidden1024>(d, grp, geo)) return 1;
+  if (plan_matches<mk::PlanHidden2048>(d, grp, geo)) return 2;
+  return 0;
+}
+const void *plan_kernel(int plan, int d) {
+  if (plan == 1) return mk::kernel_hidden1024();
+  if (plan == 2) return mk::kernel_hidden2048();
   return d == 64 ? mk::kernel_d64() : mk::kernel_d128();
 }
 
@@ -283,6 +289,64 @@ int build_forward_graph(mk_handle *h) {
 
 }  // namespace
 
+// the shape checks of mk_create (everything but the weight pointers)
+int check_shape(const mk_config &c) {
+  if (c.n_layers < 1 || c.hidden < 1 || c.n_q_heads < 1 || c.n_kv_heads < 1 || c.head_dim < 1 ||
+      c.intermediate < 1 || c.vocab < 1 || c.vocab_in < 1 || c.max_seq < 1 || c.rope_positions < 0 ||
+      !(c.rms_eps >= 0.f) || !(c.rope_theta > 0.f) || c.flags != 0)
+    return MK_ERR_INVALID_ARG;
+  if (c.head_dim != 64 && c.head_dim != 128) return MK_ERR_UNSUPPORTED;
+  if (c.n_q_heads % c.n_kv_heads) return MK_ERR_UNSUPPORTED;
+  const int grp = c.n_q_heads / c.n_kv_heads;
+  if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return MK_ERR_UNSUPPORTED;
+  if (grp * c.head_dim > mk::MAX_GRP_HD) return MK_ERR_UNSUPPORTED;
+  if (c.n_layers > mk::MAX_LAYERS) return MK_ERR_UNSUPPORTED;
+  if (c.rope_mode < 0 || c.rope_mode > 2) return MK_ERR_INVALID_ARG;
+  if (c.rope_mode != 0) {
+    if (c.mrope_sections[0] < 0 || c.mrope_sections[1] < 0 || c.mrope_sections[2] < 0 ||
+        c.mrope_sections[0] + c.mrope_sections[1] + c.mrope_sections[2] != c.head_dim / 2)
+      return MK_ERR_INVALID_ARG;
+  }
+  return MK_OK;
+}
+
+// the GEMV geometry of every phase for G CTAs: the general layouts, then a
+// fast layout for each phase where one fits
+int choose_geometry(const mk_config &c, int G, mk::GemvGeom *geo) {
+  const int H = c.hidden, d = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads, I = c.intermediate;
+  if (make_geom(H, (Hq + 2 * Hkv) * d, false, geo[mk::GV_QKV]) ||
+      make_geom(Hq * d, H, false, geo[mk::GV_O]) ||
+      make_geom(H, I, true, geo[mk::GV_GU]) ||
+      make_geom(I, H, false, geo[mk::GV_DOWN]) ||
+      make_geom(H, c.vocab, false, geo[mk::GV_LM]))
+    return MK_ERR_UNSUPPORTED;
+  // the residual stream is stored in the input layout of its readers (next
+  // layer's QKV and the LM head): both must split H the same way
+  if (geo[mk::GV_LM].fast != geo[mk::GV_QKV].fast || geo[mk::GV_LM].KPT != geo[mk::GV_QKV].KPT || geo[mk::GV_LM].TPR != geo[mk::GV_QKV].TPR)
+    return MK_ERR_UNSUPPORTED;
+
+  {
+    // fast layouts where one fits (the general ones above stay otherwise)
+    const int Ks[mk::GV_COUNT] = {H, Hq * d, H, I, H};
+    const int rows[mk::GV_COUNT] = {(Hq + 2 * Hkv) * d, H, I, H, c.vocab};
+    mk::GemvGeom fg[mk::GV_COUNT];
+    bool ok[mk::GV_COUNT];
+    for (int k = 0; k < mk::GV_COUNT; ++k) {
+      std::memset(&fg[k], 0, sizeof(fg[k]));
+      ok[k] = make_fast_geom(k, Ks[k], rows[k], G, fg[k]);
+    }
+    // the residual stream's layout is read by both the next layer's QKV and the
+    // LM head: either both take the staged layout or neither does
+    if (ok[mk::GV_QKV] != ok[mk::GV_LM]) ok[mk::GV_QKV] = ok[mk::GV_LM] = false;
+    for (int k = 0; k < mk::GV_COUNT; ++k) {
+      if (ok[k]) geo[k] = fg[k];
+      fill_shifts(geo[k]);
+      if (geo[k].fast == 2 && (geo[k].lgCH < 0 || geo[k].lgSpan < 0)) return MK_ERR_UNSUPPORTED;
+    }
+  }
+  return MK_OK;
+}
+
 extern "C" {
 
 const char *mk_error_string(int code) {
@@ -305,22 +369,8 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
   if (!cfg || !w || !out) return MK_ERR_INVALID_ARG;
   *out = nullptr;
   const mk_config c = *cfg;
-  if (c.n_layers < 1 || c.hidden < 1 || c.n_q_heads < 1 || c.n_kv_heads < 1 || c.head_dim < 1 ||
-      c.intermediate < 1 || c.vocab < 1 || c.vocab_in < 1 || c.max_seq < 1 || c.rope_positions < 0 ||
-      !(c.rms_eps >= 0.f) || !(c.rope_theta > 0.f) || c.flags != 0)
-    return MK_ERR_INVALID_ARG;
-  if (c.head_dim != 64 && c.head_dim != 128) return MK_ERR_UNSUPPORTED;
-  if (c.n_q_heads % c.n_kv_heads) return MK_ERR_UNSUPPORTED;
+  if (int rc0 = check_shape(c)) return rc0;
   const int grp = c.n_q_heads / c.n_kv_heads;
-  if (grp != 1 && grp != 2 && grp != 4 && grp != 8) return MK_ERR_UNSUPPORTED;
-  if (grp * c.head_dim > mk::MAX_GRP_HD) return MK_ERR_UNSUPPORTED;
-  if (c.n_layers > mk::MAX_LAYERS) return MK_ERR_UNSUPPORTED;
-  if (c.rope_mode < 0 || c.rope_mode > 2) return MK_ERR_INVALID_ARG;
-  if (c.rope_mode != 0) {
-    if (c.mrope_sections[0] < 0 || c.mrope_sections[1] < 0 || c.mrope_sections[2] < 0 ||
-        c.mrope_sections[0] + c.mrope_sections[1] + c.mrope_sections[2] != c.head_dim / 2)
-      return MK_ERR_INVALID_ARG;
-  }
   if (!w->embed || !w->final_norm || !w->layers) return MK_ERR_INVALID_ARG;
   if (!w->lm_head && c.vocab != c.vocab_in) return MK_ERR_INVALID_ARG;
   if (!aligned16(w->embed) || !aligned16(w->final_norm) || (w->lm_head && !aligned16(w->lm_head)))
@@ -334,17 +384,6 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
   const int H = c.hidden, d = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads, I = c.intermediate;
 
   mk::GemvGeom geo[mk::GV_COUNT];
-  if (make_geom(H, (Hq + 2 * Hkv) * d, false, geo[mk::GV_QKV]) ||
-      make_geom(Hq * d, H, false, geo[mk::GV_O]) ||
-      make_geom(H, I, true, geo[mk::GV_GU]) ||
-      make_geom(I, H, false, geo[mk::GV_DOWN]) ||
-      make_geom(H, c.vocab, false, geo[mk::GV_LM]))
-    return MK_ERR_UNSUPPORTED;
-  // the residual stream is stored in the input layout of its readers (next
-  // layer's QKV and the LM head): both must split H the same way
-  if (geo[mk::GV_LM].fast != geo[mk::GV_QKV].fast || geo[mk::GV_LM].KPT != geo[mk::GV_QKV].KPT || geo[mk::GV_LM].TPR != geo[mk::GV_QKV].TPR)
-    return MK_ERR_UNSUPPORTED;
-
   mk_handle *h = new (std::nothrow) mk_handle();
   if (!h) return MK_ERR_NO_MEMORY;
   h->cfg = c;
@@ -361,26 +400,8 @@ int mk_create(const mk_config *cfg, const mk_weights *w, mk_handle **out) {
   cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device);
   if (!coop) return fail(MK_ERR_UNSUPPORTED);
   h->G = prop.multiProcessorCount;
-  {
-    // fast layouts where one fits (the general ones above stay otherwise)
-    const int Ks[mk::GV_COUNT] = {H, Hq * d, H, I, H};
-    const int rows[mk::GV_COUNT] = {(Hq + 2 * Hkv) * d, H, I, H, c.vocab};
-    mk::GemvGeom fg[mk::GV_COUNT];
-    bool ok[mk::GV_COUNT];
-    for (int k = 0; k < mk::GV_COUNT; ++k) {
-      std::memset(&fg[k], 0, sizeof(fg[k]));
-      ok[k] = make_fast_geom(k, Ks[k], rows[k], h->G, fg[k]);
-    }
-    // the residual stream's layout is read by both the next layer's QKV and the
-    // LM head: either both take the staged layout or neither does
-    if (ok[mk::GV_QKV] != ok[mk::GV_LM]) ok[mk::GV_QKV] = ok[mk::GV_LM] = false;
-    for (int k = 0; k < mk::GV_COUNT; ++k) {
-      if (ok[k]) geo[k] = fg[k];
-      fill_shifts(geo[k]);
-      if (geo[k].fast == 2 && (geo[k].lgCH < 0 || geo[k].lgSpan < 0)) return fail(MK_ERR_UNSUPPORTED);
-    }
-  }
-  h->kernel = pick_kernel(d, Hq / Hkv, geo);
+  if (int rc1 = choose_geometry(c, h->G, geo)) return fail(rc1);
+  h->kernel = plan_kernel(pick_plan(d, Hq / Hkv, geo), d);
   // residual rows owned per CTA, and rows of every phase, must fit the static buffers
   if ((H + h->G - 1) / h->G > mk::MAX_OWN) return fail(MK_ERR_UNSUPPORTED);
   for (int k = 0; k < mk::GV_COUNT; ++k) {
@@ -770,6 +791,16 @@ int mk_decode_host(mk_handle *h, const int32_t *h_in_ids, int32_t n_in, int32_t 
     cudaGetLastError();
     return MK_ERR_CUDA;
   }
+  return MK_OK;
+}
+
+int mk_plan_for(const mk_config *cfg, int32_t n_sm, int32_t *plan) {
+  if (!cfg || !plan || n_sm < 1) return MK_ERR_INVALID_ARG;
+  if (int rc = check_shape(*cfg)) return rc;
+  mk::GemvGeom geo[mk::GV_COUNT];
+  std::memset(geo, 0, sizeof(geo));
+  if (int rc = choose_geometry(*cfg, n_sm, geo)) return rc;
+  *plan = pick_plan(cfg->head_dim, cfg->n_q_heads / cfg->n_kv_heads, geo);
   return MK_OK;
 }
 
