@@ -42,13 +42,44 @@ DECODE_SOURCES = ("mk_device.cuh", "mk_host.cu", "mk_kernels_d128.cu", "mk_kerne
                   "mk_kernels_hidden2048.cu", "mk_launch.h", "mk_params.h", "mk_plans.h", "ptx.cuh")
 
 
-def kernel_sources_sha256():
+def code_only(text):
+    """C/C++ source without comments and with whitespace runs collapsed (string
+    and character literals kept), so that editing a comment does not count as
+    changing the kernel."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def kernel_sources_sha256(read=None):
+    """Hash of the code (comments excluded) of the decode kernel's sources;
+    ``read(name)`` returns a file's text (default: the tree's csrc/)."""
     import hashlib
+    if read is None:
+        def read(name):
+            with open(os.path.join(CSRC, name)) as f:
+                return f.read()
     h = hashlib.sha256()
     for name in sorted(DECODE_SOURCES):
         h.update(name.encode())
-        with open(os.path.join(CSRC, name), "rb") as f:
-            h.update(f.read())
+        h.update(code_only(read(name)).encode())
     return h.hexdigest()
 
 

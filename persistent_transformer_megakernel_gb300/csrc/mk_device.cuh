@@ -1168,6 +1168,11 @@ static __device__ __noinline__ void merge_ticket_chunks(const Params &p, unsigne
   }
 }
 
+// One attention phase: this CTA's (kv head, chunk) units.  BLOCKS picks the
+// score loop: 8 positions per warp at a time with one multi-slot reduction
+// (the default), or one position per warp with a warp sum per head (the
+// 1.7B plan, whose staged GEMV allocates fewer registers next to it).  Both
+// are the same online softmax; their summation orders differ.
 template <int HD, int GRP, bool BLOCKS = true>
 __device__ void attention_phase(const Params &p, SmemCtl &S, unsigned char *ring, int l, int f, int cta,
                                 unsigned tag, RingPos &rp, int gp, const AttnSched &as) {

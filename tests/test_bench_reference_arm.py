@@ -37,3 +37,16 @@ def test_fewer_than_three_warmup_steps_are_refused():
     r = _bench("--steps", "1", "--warmup", "2", timeout=120)
     assert r.returncode != 0
     assert "warmup" in r.stderr
+
+
+def test_kernel_source_hash_ignores_comments():
+    # the recorded ncu traffic stays valid across comment edits, not code edits
+    import bench
+    a = 'int x = 1; // one\n/* two */ const char *s = "a//b";'
+    b = 'int x = 1;   /* other words */\nconst char *s = "a//b"; // trailing'
+    c = 'int x = 2; const char *s = "a//b";'
+    assert bench.code_only(a) == bench.code_only(b) == 'int x = 1; const char *s = "a//b";'
+    assert bench.code_only(c) != bench.code_only(a)
+    src = {n: "int f() { return 1; } // " + n for n in bench.DECODE_SOURCES}
+    moved = {n: "/* header */\nint f()\n{\n  return 1;\n}" for n in bench.DECODE_SOURCES}
+    assert bench.kernel_sources_sha256(src.get) == bench.kernel_sources_sha256(moved.get)
