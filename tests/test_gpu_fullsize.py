@@ -125,7 +125,7 @@ def test_long_context_4096_prompt_then_greedy():
     # prompt positions with its all-positions path, then continues step by step
     s = W.shape("qwen3_0p6b")
     w = W.make_weights(s, seed=0)
-    T, n_steps = 4096, 8
+    T, n_steps = 4096, 64
     prompt = W.make_prompt(s["vocab_in"], T, seed=1)
     shp = O.DecoderShape.from_dict(s)
     Wt = O.decoder.Weights(shp, w)
